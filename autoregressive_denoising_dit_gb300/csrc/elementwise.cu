@@ -1,0 +1,233 @@
+// Memory-bound kernels of the wave: adaLN-modulated LayerNorm, the latent
+// in-projection, the per-stream conditioning linears, and a dtype cast.
+#include "psv_device.cuh"
+#include "psv_kernels.h"
+
+namespace psv {
+
+namespace {
+
+constexpr int LN_THREADS = 128;
+constexpr int LN_MAXV = 12;  // float4 per thread: d <= 12 * 4 * 128 = 6144
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int i = 0; i < LN_THREADS / 32; ++i) t += red[i];
+  return t;
+}
+
+// One row per CTA; the row stays in registers between the two passes
+// (mean, then centred second moment), so h is read from HBM once.
+__global__ void __launch_bounds__(LN_THREADS)
+    ln_mod_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int d, int T,
+                  const TaskDev* __restrict__ tasks, const float* __restrict__ table,
+                  int use_fmod, int block, int shift_off, int scale_off, float eps) {
+  __shared__ float red[LN_THREADS / 32];
+  const int row = blockIdx.x;
+  const TaskDev& t = tasks[row / T];
+  const float* base = table + (use_fmod ? static_cast<int64_t>(t.fmod0)
+                                        : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
+  const float4* shift = reinterpret_cast<const float4*>(base + shift_off);
+  const float4* scale = reinterpret_cast<const float4*>(base + scale_off);
+  const float4* hr = reinterpret_cast<const float4*>(h + static_cast<int64_t>(row) * d);
+  const int nv = d >> 2;
+
+  float4 v[LN_MAXV];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < LN_MAXV; ++i) {
+    const int k = threadIdx.x + i * LN_THREADS;
+    if (k < nv) {
+      v[i] = hr[k];
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+  }
+  const float mean = block_sum(s, red) / static_cast<float>(d);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < LN_MAXV; ++i) {
+    const int k = threadIdx.x + i * LN_THREADS;
+    if (k < nv) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+      q += (a * a + b * b) + (c * c + e * e);
+    }
+  }
+  const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(d) + eps);
+  uint2* yr = reinterpret_cast<uint2*>(y + static_cast<int64_t>(row) * d);
+#pragma unroll
+  for (int i = 0; i < LN_MAXV; ++i) {
+    const int k = threadIdx.x + i * LN_THREADS;
+    if (k < nv) {
+      const float4 sh = __ldg(shift + k), sc = __ldg(scale + k);
+      uint2 o;
+      o.x = pack_bf16x2((v[i].x - mean) * rstd * (1.0f + sc.x) + sh.x,
+                        (v[i].y - mean) * rstd * (1.0f + sc.y) + sh.y);
+      o.y = pack_bf16x2((v[i].z - mean) * rstd * (1.0f + sc.z) + sh.z,
+                        (v[i].w - mean) * rstd * (1.0f + sc.w) + sh.w);
+      yr[k] = o;
+    }
+  }
+}
+
+// h[r][n] = sum_k x[r][k] W_in[n][k] + b_in[n] in f32 (K = C is small, the
+// kernel is bound by writing h).  CTA tile: 32 rows x 256 columns.
+constexpr int IP_ROWS = 32, IP_COLS = 256, IP_KC = 32;
+__global__ void __launch_bounds__(IP_COLS)
+    in_proj_kernel(const float* __restrict__ state, const __nv_bfloat16* __restrict__ w_in,
+                   const float* __restrict__ b_in, float* __restrict__ h, int M, int d, int C,
+                   int T, const TaskDev* __restrict__ tasks) {
+  __shared__ float xs[IP_ROWS][IP_KC + 1];
+  __shared__ float ws[IP_KC][IP_COLS];
+  const int r0 = blockIdx.x * IP_ROWS;
+  const int n = blockIdx.y * IP_COLS + threadIdx.x;
+  float acc[IP_ROWS];
+#pragma unroll
+  for (int i = 0; i < IP_ROWS; ++i) acc[i] = 0.0f;
+  for (int k0 = 0; k0 < C; k0 += IP_KC) {
+    for (int idx = threadIdx.x; idx < IP_ROWS * IP_KC; idx += IP_COLS) {
+      const int rr = idx / IP_KC, kk = idx % IP_KC;
+      const int row = r0 + rr, k = k0 + kk;
+      float xv = 0.0f;
+      if (row < M && k < C) {
+        const TaskDev& t = tasks[row / T];
+        xv = state[(static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k];
+      }
+      xs[rr][kk] = xv;
+    }
+    for (int idx = threadIdx.x; idx < IP_KC * IP_COLS; idx += IP_COLS) {
+      const int kk = idx / IP_COLS, nn = idx % IP_COLS;
+      const int col = blockIdx.y * IP_COLS + nn, k = k0 + kk;
+      ws[kk][nn] = (col < d && k < C)
+                       ? __bfloat162float(w_in[static_cast<int64_t>(col) * C + k])
+                       : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < IP_KC; ++kk) {
+      const float w = ws[kk][threadIdx.x];
+#pragma unroll
+      for (int i = 0; i < IP_ROWS; ++i) acc[i] = fmaf(xs[i][kk], w, acc[i]);
+    }
+    __syncthreads();
+  }
+  if (n < d) {
+    const float b = b_in[n];
+#pragma unroll
+    for (int i = 0; i < IP_ROWS; ++i) {
+      const int row = r0 + i;
+      if (row < M) h[static_cast<int64_t>(row) * d + n] = acc[i] + b;
+    }
+  }
+}
+
+// out[r][n] = act(in[r]) . W[n] + b[n] (+ add[n]).  One warp per output
+// column n, all R rows at once, so each weight row is read once.
+constexpr int CL_THREADS = 256;
+__global__ void __launch_bounds__(CL_THREADS)
+    cond_linear_kernel(const float* __restrict__ in, int R, int K,
+                       const __nv_bfloat16* __restrict__ W, const float* __restrict__ b,
+                       const float* __restrict__ add, float* __restrict__ out, int N,
+                       int silu_in) {
+  extern __shared__ float xin[];  // [R][K]
+  for (int i = threadIdx.x; i < R * K; i += blockDim.x) {
+    const float x = in[i];
+    xin[i] = silu_in ? x / (1.0f + expf(-x)) : x;
+  }
+  __syncthreads();
+  const int warps = blockDim.x / 32;
+  const int n = blockIdx.x * warps + warp_id();
+  if (n >= N) return;
+  const int lane = lane_id();
+  float acc[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+  const __nv_bfloat16* wr = W + static_cast<int64_t>(n) * K;
+  for (int k = lane * 8; k < K; k += 256) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(wr + k);
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(w2[i]);
+      w[2 * i] = f.x;
+      w[2 * i + 1] = f.y;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < R) {
+        const float* xr = xin + r * K + k;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[r] = fmaf(xr[i], w[i], acc[r]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    float v = acc[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0 && r < R) out[static_cast<int64_t>(r) * N + n] = v + b[n] + (add ? add[n] : 0.0f);
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                   int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+}  // namespace
+
+cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
+                          const TaskDev* tasks, const float* table, int use_fmod, int block,
+                          int shift_off, int scale_off, float eps, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (d % 4 != 0 || d > LN_MAXV * 4 * LN_THREADS) return cudaErrorInvalidValue;
+  ln_mod_kernel<<<M, LN_THREADS, 0, st>>>(h, y, d, T, tasks, table, use_fmod, block, shift_off,
+                                          scale_off, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_in_proj(const float* state, const __nv_bfloat16* w_in, const float* b_in,
+                           float* h, int M, int d, int C, int T, const TaskDev* tasks,
+                           cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  dim3 grid((M + IP_ROWS - 1) / IP_ROWS, (d + IP_COLS - 1) / IP_COLS);
+  in_proj_kernel<<<grid, IP_COLS, 0, st>>>(state, w_in, b_in, h, M, d, C, T, tasks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat16* W,
+                               const float* b, const float* add, float* out, int N, int silu_in,
+                               cudaStream_t st) {
+  if (R < 1 || R > 8 || K % 8 != 0) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(R) * K * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(cond_linear_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  const int warps = CL_THREADS / 32;
+  cond_linear_kernel<<<(N + warps - 1) / warps, CL_THREADS, smem, st>>>(in, R, K, W, b, add, out,
+                                                                          N, silu_in);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  f32_to_bf16_kernel<<<1184, 256, 0, st>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+}  // namespace psv

@@ -1,0 +1,83 @@
+// Host-visible launch interface of libpsv's kernels (internal to the
+// library; the public C ABI is include/psv.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace psv {
+
+struct TaskDev;
+
+// Epilogues of the tcgen05 GEMM  C[M, N] = A[M, K] * W[N, K]^T + bias.
+enum GemmEpilogue : int {
+  EPI_QKV = 0,    // RoPE on q, k; q -> Q buffer, k -> K ring, v -> V^T ring
+  EPI_RESID = 1,  // h += gate[task] * C   (gated residual, f32)
+  EPI_GELU = 2,   // u = bf16(GELU_tanh(C))
+  EPI_EULER = 3,  // x[task] += dt[task] * C   (velocity head + Euler step)
+};
+
+struct GemmParams {
+  int M, N, K;
+  int T, d, dh, H, S, B, C;
+  int block;               // transformer block b
+  int wz;                  // z coordinate of W in its [z][Npad][K] map
+  const TaskDev* tasks;
+  const float* bias;       // [N]
+  // EPI_QKV
+  __nv_bfloat16* q_out;    // [rows][d]
+  __nv_bfloat16* k_ring;   // [rings][Lr][d]
+  __nv_bfloat16* vt_ring;  // [rings][H][dh][Lp]
+  int Lr, Lp;
+  const float2* rope_local;  // [T][dh/2]   (cos, sin) of i * f_j
+  const float2* rope_base;   // [slots][dh/2] (cos, sin) of c*T * f_j
+  // EPI_RESID
+  float* h;                // [rows][d]
+  const float* mod;        // adaLN table base
+  int gate_off;            // 2d (gate1) or 5d (gate2)
+  // EPI_GELU
+  __nv_bfloat16* u;        // [rows][N]
+  // EPI_EULER
+  float* state;            // [slots][T][C]
+  int* err;
+};
+
+struct AttnParams {
+  int T, d, dh, H, S, Lr, Lp;
+  int block;
+  int n_qtiles;            // ceil(T / 128)
+  const TaskDev* tasks;
+  __nv_bfloat16* o;        // [rows][d]
+  float scale_log2;        // log2(e) / sqrt(dh)
+  int* err;
+};
+
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 4;
+size_t gemm_smem_bytes();
+size_t attn_smem_bytes(int dh);
+
+cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                        const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                             const CUtensorMap* tmV, const AttnParams& p, int n_tasks,
+                             cudaStream_t st);
+
+// Memory-bound kernels.
+// y = bf16(LN(h) * (1 + scale) + shift), per row; shift/scale of the row's
+// task at mod + task.mod0 + block*6d + {shift_off, scale_off} (or fmod).
+cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
+                          const TaskDev* tasks, const float* table, int use_fmod, int block,
+                          int shift_off, int scale_off, float eps, cudaStream_t st);
+// h = x W_in^T + b_in, x gathered from each task's latent state slot.
+cudaError_t launch_in_proj(const float* state, const __nv_bfloat16* w_in, const float* b_in,
+                           float* h, int M, int d, int C, int T, const TaskDev* tasks,
+                           cudaStream_t st);
+// out[r][n] = act(in[r]) . W[n] + b[n] (+ add[n]), r < R; act = SiLU or id.
+cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat16* W,
+                               const float* b, const float* add, float* out, int N,
+                               int silu_in, cudaStream_t st);
+cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t st);
+
+}  // namespace psv

@@ -1,0 +1,452 @@
+"""Steady-state serving benchmark of the autoregressive-denoising DiT wave path.
+
+One step = one wave: every ready (chunk, step) task of every stream through
+in-proj, all B blocks (LN1+mod, QKV+RoPE+KV append, window attention,
+out-proj+gated residual, LN2+mod, up+GELU, down+gated residual) and the
+final adaLN + velocity head + Euler update.  In a steady wave (every task at
+a full KV window) each stream emits one chunk, so ms/step = per-stream
+ms/chunk and value = aggregate chunks/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+N > 1 (under torchrun): independent replicas, one per GPU (the path has no
+exchange step); value = chunks of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "steady-state ms/chunk & chunks/s on 1 GB300; tensor-pipe % of BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_name(cfg_name: str, cfg: dict) -> str:
+    return (f"{cfg_name}: {cfg['B']} blocks x {cfg['S']} steps, d={cfg['d']}, "
+            f"{cfg['H']}x{cfg['dh']} heads, F={cfg['F']}, C={cfg['C']}, T={cfg['T']}, "
+            f"W={cfg['W']}, {cfg['n_streams']} stream(s) x {cfg['n_chunks']} chunks")
+
+
+def wave_flops(cfg: dict) -> float:
+    """Algorithmic FLOPs of one steady wave (every task at a full window)."""
+    n_task = cfg["S"] * cfg["n_streams"]
+    M = n_task * cfg["T"]
+    d, F, B, C, T = cfg["d"], cfg["F"], cfg["B"], cfg["C"], cfg["T"]
+    Lk = (cfg["W"] + 1) * T
+    gemm = 2.0 * M * B * (4 * d * d + 2 * d * F)
+    attn = 4.0 * T * Lk * d * n_task * B
+    io = 4.0 * M * C * d
+    return gemm + attn + io
+
+
+def wave_bytes(cfg: dict) -> float:
+    """Algorithmic HBM bytes of one steady wave: bf16 block weights once,
+    window KV reads, own KV writes, latent in/out."""
+    n_task = cfg["S"] * cfg["n_streams"]
+    d, F, B, C, T, W = cfg["d"], cfg["F"], cfg["B"], cfg["C"], cfg["T"], cfg["W"]
+    weights = B * (4 * d * d + 2 * d * F) * 2.0 + 2.0 * C * d
+    kv = n_task * B * (W * T * d * 2 * 2 + T * d * 2 * 2)
+    latent = n_task * T * C * 4 * 2.0
+    return weights + kv + latent
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                return json.load(f), "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks: dict, key: str):
+    for k in (key, key.replace("_sustained", "")):
+        if k in peaks and isinstance(peaks[k], (int, float)):
+            return float(peaks[k])
+        for v in peaks.values():
+            if isinstance(v, dict) and k in v and isinstance(v[k], (int, float)):
+                return float(v[k])
+    return FALLBACK_PEAKS[key]
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"psv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "psv" else "gloo"
+        if backend == "nccl":
+            import torch
+
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_wave_sample(cfg: dict, budget_s: float, min_blocks: int = 1):
+    """Time the f32 oracle on blocks of one steady wave (every task with a full
+    window, inputs drawn at the workload's shapes) until ``budget_s`` passed.
+    Returns (seconds per whole wave, blocks timed, threads)."""
+    from oracle import model as M
+
+    rng = np.random.default_rng(0)
+    d, T, W, S = cfg["d"], cfg["T"], cfg["W"], cfg["S"]
+    n_task = S * cfg["n_streams"]
+    specs = dict(synth.block_specs(cfg))
+    bw = {k: (rng.standard_normal(s, dtype=np.float32) * 0.02 if k.endswith("_w")
+              else np.zeros(s, np.float32)) for k, s in specs.items()}
+    tasks = []
+    for i in range(n_task):
+        c = W + (S - 1) - (i % S)
+        tasks.append(dict(
+            h=rng.standard_normal((T, d), dtype=np.float32),
+            mod=rng.standard_normal(6 * d, dtype=np.float32) * 0.1,
+            pos=M.positions(cfg, c),
+            window=[(rng.standard_normal((T, d), dtype=np.float32),
+                     rng.standard_normal((T, d), dtype=np.float32)) for _ in range(W)]))
+    t0 = time.perf_counter()
+    n_blocks = 0
+    while True:
+        for t in tasks:
+            M.block_forward(cfg, bw, t["mod"], t["h"], t["pos"], t["window"])
+        n_blocks += 1
+        el = time.perf_counter() - t0
+        if (el >= budget_s and n_blocks >= min_blocks) or n_blocks >= cfg["B"]:
+            break
+    per_block = el / n_blocks
+    threads = os.cpu_count() or 1
+    return per_block * cfg["B"], n_blocks, threads
+
+
+def run_reference(args, cfg_name, cfg, world, rank):
+    if rank != 0:
+        return 0
+    per_step = []
+    budget = max(0.5, args.ref_budget)
+    steps_total = args.warmup + args.steps
+    for i in range(steps_total):
+        wave_s, nb, threads = oracle_wave_sample(cfg, budget / steps_total, 1)
+        if i >= args.warmup:
+            per_step.append(wave_s)
+    wave_s = float(np.mean(per_step))
+    value = cfg["n_streams"] / wave_s
+    sample = (f"f32 numpy oracle, one transformer block of a steady {cfg['S'] * cfg['n_streams']}-task "
+              f"wave per step (all tasks at a full W={cfg['W']} window), scaled x{cfg['B']} blocks")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wave_s * 1e3, "ms_per_chunk": wave_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_name(cfg_name, cfg), "parallelism": "replicas",
+                   "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU path
+
+def run_psv(args, cfg_name, cfg, world, rank, local):
+    import torch
+
+    from autoregressive_denoising_dit_gb300 import Session, _psv as P
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    S, W, T, C = cfg["S"], cfg["W"], cfg["T"], cfg["C"]
+    n_st = cfg["n_streams"]
+    fill = W + S - 1                       # waves before the first steady wave
+    prof_waves = 3
+    n_resident = fill + args.warmup + args.steps + prof_waves
+    inflight = max(cfg["n_chunks"], n_resident) + S + 8
+    sess = Session(cfg, max_streams=n_st, max_inflight=inflight)
+    sess.load_device_weights(synth.iter_device_weights(cfg, seed=0, device=f"cuda:{local}"))
+    torch.cuda.synchronize()
+    streams = synth.make_streams(cfg)
+    sids = [sess.open_stream(st.cond) for st in streams]
+    # resident inputs: every chunk of the device-timed phase submitted up front
+    for c in range(n_resident):
+        for st, sid in zip(streams, sids):
+            sess.submit(sid, st.noise(c))
+    for _ in range(fill + args.warmup):
+        sess.run_wave()
+    sess.sync(600000)
+    torch.cuda.synchronize()
+
+    stream = sess.torch_stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        n = sess.run_wave()
+        ev[k][1].record(stream)
+        assert n == S * n_st, f"wave {k} is not steady ({n} tasks)"
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    per_wave = sorted(a.elapsed_time(b) for a, b in ev)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_step = total_ms / args.steps
+    value = world * n_st * args.steps / (total_ms / 1e3)
+
+    # per-kernel timing pass (eager launches bracketed by events)
+    P.psv_set_profiling(sess.ctx, True)
+    for _ in range(prof_waves):
+        sess.run_wave()
+    times = P.psv_kernel_times(sess.ctx)
+    P.psv_set_profiling(sess.ctx, False)
+    sess.sync(600000)
+
+    # drain, then the end-to-end phase through host buffers
+    while sess.run_wave():
+        pass
+    sess.sync(600000)
+    buf = np.empty((T, C), dtype=np.float32)
+    for sid in sids:
+        while sess.poll(sid, buf) is not None:
+            pass
+    next_chunk = n_resident
+    e2e_warm = S - 1 + 3
+    e2e_steps = args.steps
+
+    def e2e_step(c):
+        for st, sid in zip(streams, sids):
+            sess.submit(sid, st.noise(c))
+        sess.run_wave()
+        out = 0
+        for sid in sids:
+            while True:
+                got = sess.poll(sid, buf)
+                if got is not None:
+                    out += 1
+                    break
+        return out
+
+    for _ in range(e2e_warm):  # pipeline fill: the first S-1 waves emit nothing
+        for st, sid in zip(streams, sids):
+            sess.submit(sid, st.noise(next_chunk))
+        next_chunk += 1
+        sess.run_wave()
+        for sid in sids:
+            sess.poll(sid, buf)
+    sess.sync(600000)
+    # catch up so each timed step emits exactly one chunk per stream
+    for sid in sids:
+        while sess.poll(sid, buf) is not None:
+            pass
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step(next_chunk)
+        next_chunk += 1
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - w0, world, dev)
+    e2e_value = world * n_st * e2e_steps / e2e_s
+    n_task = S * n_st
+    h2d = n_st * T * C * 4 + n_task * 48 + n_st * (cfg["dh"] // 2) * 8
+    d2h = n_st * (T * C * 4 + 4)
+
+    # roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    dom = max(times.items(), key=lambda kv: kv[1]["total_ms"])
+    name, t = dom
+    per_launch_ms = t["total_ms"] / max(1, t["launches"])
+    tensor_kernel = name.startswith("gemm") or name == "attention"
+    if tensor_kernel:
+        achieved = t["flops"] / max(1, t["launches"]) / (per_launch_ms / 1e3) / 1e12
+        peak = peak_value(peaks, "bf16_tflops_sustained")
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    else:
+        achieved = t["bytes"] / max(1, t["launches"]) / (per_launch_ms / 1e3) / 1e9
+        peak = peak_value(peaks, "hbm_gbs")
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    roof["kernel"] = name
+    roof["peak_source"] = f"{peak_src} ({'sustained bf16' if tensor_kernel else 'HBM copy'})"
+    roof["traffic"] = None
+    tfile = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(tfile):
+        try:
+            with open(tfile) as f:
+                tr = json.load(f)
+            if name in tr.get("kernels", {}) and tr.get("config") == cfg_name:
+                roof["traffic"] = tr["kernels"][name]["bytes_per_launch"]
+        except Exception:
+            pass
+    flops = wave_flops(cfg)
+    bytes_ = wave_bytes(cfg)
+    bf16_peak = peak_value(peaks, "bf16_tflops_sustained") * 1e12
+    hbm_peak = peak_value(peaks, "hbm_gbs") * 1e9
+    roof_ms = max(flops / bf16_peak, bytes_ / hbm_peak) * 1e3
+    kernels = {k: {"launches": v["launches"], "ms_per_launch": v["total_ms"] / max(1, v["launches"]),
+                   "share": v["total_ms"] / max(1e-9, sum(x["total_ms"] for x in times.values()))}
+               for k, v in times.items() if v["launches"]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "chunks/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_chunk": ms_step, "ms_per_chunk_p50": per_wave[len(per_wave) // 2],
+        "ms_per_chunk_p90": per_wave[min(len(per_wave) - 1, int(0.9 * len(per_wave)))],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights, N(0,1) noise/cond)",
+        "config": {"workload": workload_name(cfg_name, cfg), "tasks_per_wave": n_task,
+                   "rows_per_wave": n_task * T, "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2 (bf16 weights + KV rings read every wave)",
+                   "graphs": True},
+        "wave_roofline": {"flops_per_wave": flops, "bytes_per_wave": bytes_, "roofline_ms": roof_ms,
+                          "frac": roof_ms / ms_step,
+                          "tensor_tflops": flops / (ms_step / 1e3) / 1e12,
+                          "tensor_frac_of_bf16_peak": flops / (ms_step / 1e3) / bf16_peak,
+                          "peak_source": peak_src},
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": e2e_value, "unit": "chunks/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s / e2e_steps * 1e3},
+        "gpu_launches": (3 + 7 * cfg["B"]) * args.steps,
+        "clocks": clk,
+    }
+    sess.close()
+    if rank == 0 and not args.no_cpu_baseline:
+        wave_s, nb, threads = oracle_wave_sample(cfg, args.ref_budget, 1)
+        line["cpu_baseline"] = {
+            "value": cfg["n_streams"] / wave_s, "unit": "chunks/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"f32 numpy oracle on {nb} transformer block(s) of one steady "
+                       f"{n_task}-task wave, scaled x{cfg['B'] / nb:.1f} to the whole wave")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["psv", "reference"], default="psv")
+    ap.add_argument("--config", default="wan21_1p3b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--ref-budget", type=float, default=15.0,
+                    help="seconds of CPU time for the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = synth.config(args.config)
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, args.config, cfg, world, rank)
+        return run_psv(args, args.config, cfg, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * psv.h — C ABI of libpsv: single-GPU serving of autoregressive-denoising
+ * DiT world models on GB300 (sm_103a).
+ *
+ * The problem these calls serve (AREX article "vLLM 与 Physis-AI 联合介绍
+ * PhysisServe 推理系统", §难题 and §三层设计; BAAI announcement
+ * "智源悟界·PhysisServe：首个兼顾智能与高频吞吐的物理 AI 推理系统",
+ * §新一代物理 AI 的基础设施 Fig. 1 and §PhysisServe Fig. 2–3):
+ *   - a stream produces latent chunks; every chunk starts from pure noise
+ *     and is denoised over S steps;
+ *   - at step s and transformer block b a chunk attends to its own tokens
+ *     plus the still-noisy keys/values that the W preceding chunks left at
+ *     the same (block, step), so chunk c step s may run once chunk c step
+ *     s-1 and chunk c-1 step s are done;
+ *   - every ready (chunk, step) task of every stream is time-shared on the
+ *     one GPU: a "wave" runs them all, block by block, each block as one
+ *     batched launch per operation (same-block batching, Fig. 3 right).
+ *
+ * Conventions
+ *   - every call returns 0 (PSV_OK) or a negative PSV_E* code; on error
+ *     psv_last_error() describes it; PSV_ECUDA and PSV_EDEVICE are sticky;
+ *   - the library never frees caller memory; host inputs are copied before
+ *     a call returns, so the caller may reuse its buffers at once;
+ *   - device work is issued on the caller's CUDA stream (given at create)
+ *     and is asynchronous unless a call says otherwise;
+ *   - all matrices are row-major; linear weights use the [out, in] layout.
+ */
+#ifndef PSV_H
+#define PSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PSV_OK          0
+#define PSV_EINVAL     (-1)  /* bad argument, shape or state                   */
+#define PSV_ENOMEM     (-2)  /* arena too small / host allocation failed       */
+#define PSV_EAGAIN     (-3)  /* nothing to return yet / queue full: retry later */
+#define PSV_ETIMEDOUT  (-4)  /* psv_sync deadline passed (host-side polling)    */
+#define PSV_ECUDA      (-5)  /* a CUDA runtime call failed (sticky)             */
+#define PSV_EDEVICE    (-6)  /* a kernel raised its error word (sticky)         */
+
+/* ---- create flags -------------------------------------------------------- */
+#define PSV_FLAG_PLAN_ONLY   1  /* host scheduler only: no device, no arena     */
+#define PSV_FLAG_SEQUENTIAL  2  /* one task per wave, lowest (stream, chunk,
+                                   step) first: strictly sequential order       */
+
+/* ---- model description --------------------------------------------------
+ * B blocks, S Euler steps (t_s = 1 - s/S), model width d = H*dh, MLP width
+ * F, latent channels C (already patchified), T tokens per chunk, KV window
+ * W (a chunk sees its own KV plus that of the W preceding chunks).
+ * Requirements: d % 128 == 0, F % 64 == 0, dh in {32, 64, 128}, T >= 1,
+ * W >= 0, 1 <= S <= 8, t_embed % 2 == 0 and <= 1024, C <= 256.
+ * max_inflight: chunks of one stream alive at once (submitted and not yet
+ * polled); 0 selects S + 4. */
+typedef struct psv_model_desc {
+  int32_t B, S, d, H, dh, F, C, T, W;
+  int32_t max_streams;
+  int32_t max_inflight;
+  int32_t t_embed;      /* sinusoidal timestep-embedding width (256)       */
+  float   ln_eps;       /* LayerNorm epsilon (1e-6)                        */
+  float   rope_theta;   /* RoPE base (1e4)                                 */
+  int32_t flags;        /* PSV_FLAG_*                                      */
+} psv_model_desc;
+
+/* ---- weights --------------------------------------------------------------
+ * Global tensors (block = -1):
+ *   IN_W [d, C]  IN_B [d]        latent -> residual stream
+ *   T1_W [d, t_embed] T1_B [d]   time MLP, first layer (SiLU after it)
+ *   T2_W [d, d]  T2_B [d]        time MLP, second layer
+ *   FMOD_W [2d, d] FMOD_B [2d]   final adaLN: [shift_f, scale_f]
+ *   OUT_W [C, d] OUT_B [C]       velocity head
+ * Per block b (block = b):
+ *   QKV_W [3d, d] QKV_B [3d]     rows [q | k | v], head h = rows h*dh..
+ *   O_W [d, d]   O_B [d]
+ *   UP_W [F, d]  UP_B [F]        GELU (tanh form) after it
+ *   DOWN_W [d, F] DOWN_B [d]
+ *   MOD_W [6d, d] MOD_B [6d]     adaLN: [shift1, scale1, gate1, shift2,
+ *                                scale2, gate2] = MOD_W SiLU(e_s) + MOD_B
+ * Matrices are stored in bf16 (f32 input is rounded to nearest even);
+ * biases are stored in f32.  All tensors must be loaded before
+ * psv_open_stream. */
+enum {
+  PSV_W_IN_W = 0, PSV_W_IN_B, PSV_W_T1_W, PSV_W_T1_B, PSV_W_T2_W, PSV_W_T2_B,
+  PSV_W_FMOD_W, PSV_W_FMOD_B, PSV_W_OUT_W, PSV_W_OUT_B,
+  PSV_W_QKV_W = 16, PSV_W_QKV_B, PSV_W_O_W, PSV_W_O_B, PSV_W_UP_W, PSV_W_UP_B,
+  PSV_W_DOWN_W, PSV_W_DOWN_B, PSV_W_MOD_W, PSV_W_MOD_B
+};
+#define PSV_DTYPE_F32   0
+#define PSV_DTYPE_BF16  1
+#define PSV_LOC_HOST    0
+#define PSV_LOC_DEVICE  1
+
+typedef struct psv_weight {
+  int32_t id;          /* PSV_W_*                                   */
+  int32_t block;       /* -1 for global tensors, else 0..B-1        */
+  const void* data;    /* host or device pointer, see location      */
+  int32_t dtype;       /* PSV_DTYPE_F32 or PSV_DTYPE_BF16           */
+  int32_t location;    /* PSV_LOC_HOST or PSV_LOC_DEVICE            */
+  int64_t numel;       /* must equal the tensor's element count     */
+} psv_weight;
+
+/* One scheduled task, for introspection (psv_wave_plan). */
+typedef struct psv_task {
+  int32_t stream;      /* stream id                                          */
+  int32_t chunk;       /* chunk index c within the stream                    */
+  int32_t step;        /* denoising step s                                   */
+  int32_t slot;        /* KV ring slot the task writes: c mod (W+1)          */
+  int32_t kv_len;      /* keys the task attends to: (min(c, W) + 1) * T      */
+  int32_t row_off;     /* first row of the task in the wave's batch          */
+  int32_t state_slot;  /* latent state slot holding x of this chunk          */
+} psv_task;
+
+/* Per-kernel timing, filled when profiling is on (psv_set_profiling). */
+typedef struct psv_kernel_time {
+  char    name[32];
+  int64_t launches;
+  double  total_ms;
+  double  flops;       /* algorithmic FLOPs of all launches              */
+  double  bytes;       /* algorithmic HBM bytes of all launches          */
+} psv_kernel_time;
+
+typedef struct psv_ctx psv_ctx;
+
+/* Device bytes psv_create needs for this description (weights, KV rings
+ * for max_streams, activations for the largest wave, latent state, tables). */
+int psv_arena_bytes(const psv_model_desc* desc, size_t* bytes);
+
+/* Create a context.  dev_arena/arena_bytes: caller-owned device memory of at
+ * least psv_arena_bytes() bytes, 1024-byte aligned, used until psv_destroy;
+ * cuda_stream: caller-owned cudaStream_t all device work is issued on
+ * (NULL = legacy default stream).  With PSV_FLAG_PLAN_ONLY the arena and
+ * stream are ignored (may be NULL) and no CUDA call is made.
+ * Errors: PSV_EINVAL (bad shape), PSV_ENOMEM (arena too small), PSV_ECUDA. */
+int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena_bytes,
+               void* cuda_stream, psv_ctx** out);
+
+/* Copy n tensors into the arena (see the weight table above).  Synchronous
+ * with respect to the host buffers.  Errors: PSV_EINVAL (unknown id, wrong
+ * numel or dtype), PSV_ECUDA. */
+int psv_load_weights(psv_ctx* ctx, const psv_weight* w, int n);
+
+/* Open a stream with conditioning vector cond (host, f32 [d]).  Builds the
+ * stream's adaLN tables on the device: for every step s,
+ * e_s = T2 SiLU(T1 emb(t_s) + b1) + b2 + cond, mod[s][b] = MOD_W,b SiLU(e_s)
+ * + MOD_B,b, fmod[s] = FMOD_W SiLU(e_s) + FMOD_B.  Stream ids are assigned
+ * lowest-free-first.  Errors: PSV_EAGAIN (max_streams open), PSV_EINVAL. */
+int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id);
+
+/* Submit the next chunk of a stream: noise (host, f32 [T, C], the chunk's
+ * x_0).  Chunks are numbered 0, 1, ... in submission order.  Errors:
+ * PSV_EAGAIN (max_inflight chunks alive: poll first), PSV_EINVAL. */
+int psv_submit_chunk(psv_ctx* ctx, int stream_id, const float* noise);
+
+/* Run one wave: every task whose dependencies are met, all streams batched
+ * block by block.  Asynchronous on the context stream.  *n_tasks = tasks
+ * run (0 = nothing ready; no device work issued). */
+int psv_run_wave(psv_ctx* ctx, int* n_tasks);
+
+/* Return the oldest finished, not yet returned chunk of a stream: copies
+ * its final latent x_S (f32 [T, C]) to host `out` and its index to
+ * *chunk_idx.  Non-blocking: PSV_EAGAIN if that chunk's wave has not
+ * finished on the device (or no chunk of the stream has been run to its
+ * last step).  Checks the device error word: PSV_EDEVICE if set. */
+int psv_poll_chunk(psv_ctx* ctx, int stream_id, float* out, int64_t* chunk_idx);
+
+/* Wait (host-side polling, no device spin) until all issued work is done.
+ * timeout_ms < 0 waits without deadline.  PSV_ETIMEDOUT on deadline. */
+int psv_sync(psv_ctx* ctx, int timeout_ms);
+
+/* The task list the next psv_run_wave would run (no state change).
+ * Writes min(n, cap) entries; *n = number of ready tasks. */
+int psv_wave_plan(psv_ctx* ctx, psv_task* buf, int cap, int* n);
+
+/* Close a stream; its id and rings become free.  Queued work is not
+ * cancelled: call after its chunks were polled. */
+int psv_close_stream(psv_ctx* ctx, int stream_id);
+
+/* Destroy the context (synchronises the stream first).  NULL is a no-op. */
+void psv_destroy(psv_ctx* ctx);
+
+/* Last error message of this context ("" if none); NULL ctx gives the
+ * message of the last failed psv_create. */
+const char* psv_last_error(const psv_ctx* ctx);
+
+/* ---- executor controls and introspection -------------------------------- */
+
+/* Replay each wave shape (task count) as a CUDA graph (default on). */
+int psv_set_graphs(psv_ctx* ctx, int enabled);
+
+/* Record CUDA events around every kernel launch (forces eager launches
+ * while on).  psv_kernel_times returns per-kernel totals since enabling;
+ * it synchronises the stream.  Writes min(cap, kinds) entries, *n = kinds. */
+int psv_set_profiling(psv_ctx* ctx, int enabled);
+int psv_kernel_times(psv_ctx* ctx, psv_kernel_time* out, int cap, int* n);
+
+/* Debug tap for parity tests: during the next psv_run_wave (run eagerly),
+ * copy the residual stream h (f32 [n_tasks*T, d], rows in task order) into
+ * the caller's device buffers h_in (before block `block`) and h_out (after
+ * it).  Cleared after that wave. */
+int psv_debug_tap(psv_ctx* ctx, int block, float* h_in, float* h_out);
+
+/* Debug read of one KV ring (stream, block, step) into host f32 buffers:
+ * k [(W+1)*T, d] and v [(W+1)*T, d], rows = slot*T + token.  Synchronous. */
+int psv_debug_read_kv(psv_ctx* ctx, int stream_id, int block, int step,
+                      float* k, float* v);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSV_H */

@@ -125,24 +125,28 @@ def step_times(S: int) -> np.ndarray:
     return np.array([1.0 - s / S for s in range(S + 1)], dtype=np.float64)
 
 
-def conditioning(cfg: dict, g: dict, blocks: list, cond: np.ndarray, dtype=np.float64):
+def conditioning(cfg: dict, g: dict, blocks, cond: np.ndarray, dtype=np.float64):
     """Per-stream modulation tables, readings <1>-<5>.
 
     Returns mod [S, B, 6d] and fmod [S, 2d]: for each step s,
     temb = W_t2 SiLU(W_t1 emb(t_s) + b_t1) + b_t2, e = temb + cond,
     mod[s][b] = W_mod,b SiLU(e) + b_mod,b, fmod[s] = W_fmod SiLU(e) + b_fmod.
+    ``blocks`` is a list of all block weight dicts, or a dict {b: weights}
+    for a subset (rows of the other blocks are left as NaN).
     """
     S, B, d = cfg["S"], cfg["B"], cfg["d"]
     ts = step_times(S)
-    mod = np.empty((S, B, 6 * d), dtype=dtype)
+    items = blocks.items() if isinstance(blocks, dict) else enumerate(blocks)
+    items = list(items)
+    mod = np.full((S, B, 6 * d), np.nan, dtype=dtype)
     fmod = np.empty((S, 2 * d), dtype=dtype)
     cond = cond.astype(dtype)
     for s in range(S):
         emb = timestep_embedding(ts[s], cfg["t_embed"]).astype(dtype)
         temb = linear(silu(linear(emb, g["t1_w"], g["t1_b"])), g["t2_w"], g["t2_b"])
         se = silu(temb + cond)
-        for b in range(B):
-            mod[s, b] = linear(se, blocks[b]["mod_w"], blocks[b]["mod_b"])
+        for b, bw in items:
+            mod[s, b] = linear(se, bw["mod_w"], bw["mod_b"])
         fmod[s] = linear(se, g["fmod_w"], g["fmod_b"])
     return mod, fmod
 

@@ -153,3 +153,26 @@ class StreamInputs:
 def make_streams(cfg: dict, n_streams: int | None = None):
     n = cfg["n_streams"] if n_streams is None else n_streams
     return [StreamInputs(cfg, i) for i in range(n)]
+
+
+def iter_device_weights(cfg: dict, seed: int = 0, device: str = "cuda"):
+    """Yield (block, name, torch tensor) drawn on the GPU with torch's seeded
+    Philox generator: matrices N(0, 0.02) as bf16, biases zero f32.
+
+    Same shapes, order and distribution as ``iter_weights`` but a different
+    generator (the values differ); used where only the timing matters, to
+    avoid drawing billions of numbers on the host.
+    """
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    specs = [(-1, n, s) for n, s in global_specs(cfg)]
+    for b in range(cfg["B"]):
+        specs += [(b, n, s) for n, s in block_specs(cfg)]
+    for b, name, shape in specs:
+        if name.endswith("_b"):
+            yield b, name, torch.zeros(shape, dtype=torch.float32, device=device)
+        else:
+            w = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+            yield b, name, (w * WEIGHT_STD).to(torch.bfloat16)

@@ -373,8 +373,15 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
         try:
             with open(tfile) as f:
                 tr = json.load(f)
-            if name in tr.get("kernels", {}) and tr.get("config") == cfg_name:
-                roof["traffic"] = tr["kernels"][name]["bytes_per_launch"]
+            ent = tr.get("kernels", {}).get(name)
+            if ent and tr.get("config") == cfg_name:
+                import hashlib
+
+                with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+                    sha = hashlib.sha256(f.read()).hexdigest()[:16]
+                # counters of an older build of the kernel do not count
+                if sha == ent["sha256_16"]:
+                    roof["traffic"] = ent["bytes_per_launch"]
         except Exception:
             pass
     flops = wave_flops(cfg)
@@ -432,10 +439,14 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=15.0,
                     help="seconds of CPU time for the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blocks", type=int, default=None,
+                    help="override the block count (profiling aid: per-block shapes are unchanged)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = synth.config(args.config)
+    if args.blocks:
+        cfg["B"] = args.blocks
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":

@@ -9,14 +9,22 @@
 // window is the ring prefix [0, kv_len) in physical slot order (softmax is
 // invariant to key order).  No mask: a chunk is bidirectional.
 //
-// One CTA per (task, head, 128-query tile), warp-specialised:
-//   warp 0      TMA: Q once, then K and V^T tiles of 128 keys (2 stages)
-//   warp 1      TMEM allocator + MMA issuer: S = Q K^T into one of two TMEM
-//               S buffers (S_{j+1} overlaps softmax j), O += P V into TMEM
-//   warps 2..5  softmax, one query row per thread: online max/sum in the
-//               log2 domain, lazy O rescale (only when the running max grows
-//               by more than 8, i.e. a factor 256), P written as bf16 to
-//               shared memory in the swizzled K-major layout the MMA reads.
+// One CTA per (task, head, pair of 128-query tiles); both query tiles share
+// every K / V^T tile loaded.  Warp roles (320 threads):
+//   warp 0      TMA: Q0, Q1 once, then K and V^T tiles of 128 keys (2 stages)
+//   warp 1      TMEM allocator + MMA issuer, per key tile j:
+//                 PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+//               so the tensor core always has the other tile's work while a
+//               softmax warpgroup runs (ping-pong)
+//   warps 2..5  softmax of query tile 0, warps 6..9 of tile 1: one row per
+//               thread; online max/sum in the log2 domain, lazy O rescale
+//               (only when the running max grows by more than 2^8), P in
+//               bf16 written to TMEM over its own S columns and consumed by
+//               the P.V MMA straight from TMEM.
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+dh), O1 [384,..).
+// tcgen05 MMAs of one issuing thread execute in order, so S_{i,j+1} (issued
+// after PV_{i,j}) only overwrites P_{i,j} once it was consumed, and when
+// S_{i,j+1} is complete O_i is stable for the softmax warps to rescale.
 #include "psv_device.cuh"
 #include "psv_kernels.h"
 
@@ -24,30 +32,28 @@ namespace psv {
 
 namespace {
 
-constexpr int QT = 128;   // queries per CTA
+constexpr int QT = 128;   // queries per tile (two tiles per CTA)
 constexpr int KT = 128;   // keys per tile
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kThreads = 320;
 
 template <int DH>
 struct AttnCfg {
-  static constexpr int AW = DH < 64 ? DH : 64;          // elements per swizzle row
-  static constexpr int ROWB = AW * 2;                   // bytes per swizzle row
-  static constexpr int NA = DH / AW;                    // atoms along dh
+  static constexpr int AW = DH < 64 ? DH : 64;  // elements per swizzle row
+  static constexpr int ROWB = AW * 2;           // bytes per swizzle row
+  static constexpr int NA = DH / AW;            // atoms along dh
   static constexpr int Q_BYTES = QT * DH * 2;
   static constexpr int K_BYTES = KT * DH * 2;
-  static constexpr int V_BYTES = DH * KT * 2;           // V^T tile [DH][128 keys]
-  static constexpr int P_BYTES = QT * KT * 2;
+  static constexpr int V_BYTES = DH * KT * 2;   // V^T tile [DH][128 keys]
   static constexpr int Q_ATOM = QT * ROWB;
   static constexpr int K_ATOM = KT * ROWB;
-  static constexpr int V_ATOM = DH * 128;               // [DH rows][64 keys]
-  static constexpr int P_ATOM = QT * 128;               // [128 rows][64 keys]
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int V_ATOM = DH * 128;       // [DH rows][64 keys]
+  static constexpr int OFF_Q = 0;               // two query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int N_BARS = 12;
+  static constexpr int OFF_BAR = OFF_V + 2 * V_BYTES;
+  static constexpr int N_BARS = 14;
   static constexpr size_t SMEM = 1024 + OFF_BAR + N_BARS * 8 + 16;
 };
 
@@ -57,8 +63,53 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// D(tmem) (+)= A(tmem, bf16 packed 2 per column) x B(smem descriptor).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0, x1) * s + (b, b) on the packed f32x2 path.
+__device__ __forceinline__ void ffma2(float& x0, float& x1, float s, float b) {
+  uint64_t x, sv, bv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bv) : "f"(b));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x) : "l"(sv), "l"(bv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x));
+}
+
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  uint64_t a, b;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+  asm("add.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+
 template <int DH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -69,30 +120,32 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sQ = smem + Cfg::OFF_Q;
   uint8_t* sK = smem + Cfg::OFF_K;
   uint8_t* sV = smem + Cfg::OFF_V;
-  uint8_t* sP = smem + Cfg::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
+  uint64_t* k_full = bars + 1;    // [2] stage
+  uint64_t* v_full = bars + 3;    // [2] stage
+  uint64_t* kv_empty = bars + 5;  // [2] stage
+  uint64_t* s_full = bars + 7;    // [2] query tile
+  uint64_t* p_full = bars + 9;    // [2] query tile (4 warps arrive)
+  uint64_t* o_done = bars + 11;   // [2] query tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::N_BARS);
 
   const int warp = warp_id(), lane = lane_id();
+  // Full query pairs first, the task tails (one valid tile or less) last.
+  const int n_tasks = gridDim.x / (p.n_qtiles * p.H);
   const int work = blockIdx.x;
-  const int qt = work % p.n_qtiles;
-  const int head = (work / p.n_qtiles) % p.H;
-  const int ti = work / (p.n_qtiles * p.H);
+  const int ti = work % n_tasks;
+  const int head = (work / n_tasks) % p.H;
+  const int pair = work / (n_tasks * p.H);
   const TaskDev task = p.tasks[ti];
   const int ring = task.ring0 + p.block * p.S;
   const int kv_len = task.kv_len;
   const int nT = (kv_len + KT - 1) / KT;
-  const int qrow0 = task.row0 + qt * QT;  // first query row in the wave batch
+  const int qrow0 = task.row0 + pair * 2 * QT;  // first query row in the wave batch
+  const bool has_q1 = pair * 2 * QT + QT < p.T;
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 7 || i == 8 || i == 9) ? 4 : 1);
+    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 4 : 1);
     fence_mbar_init();
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
@@ -103,17 +156,22 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 2 * KT;  // O accumulator columns [256, 256 + DH)
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       int issued = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, Cfg::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, Cfg::Q_BYTES * (has_q1 ? 2 : 1));
 #pragma unroll
       for (int a = 0; a < Cfg::NA; ++a)
         tma_load_2d(sQ + a * Cfg::Q_ATOM, &tmQ, q_full, head * DH + a * Cfg::AW, qrow0);
+      if (has_q1) {
+#pragma unroll
+        for (int a = 0; a < Cfg::NA; ++a)
+          tma_load_2d(sQ + Cfg::Q_BYTES + a * Cfg::Q_ATOM, &tmQ, q_full, head * DH + a * Cfg::AW,
+                      qrow0 + QT);
+      }
       for (int j = 0; j < nT; ++j) {
         const int st = j & 1;
         const uint32_t use = j >> 1;
@@ -121,25 +179,30 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[st], Cfg::K_BYTES + Cfg::V_BYTES);
         uint8_t* k_dst = sK + st * Cfg::K_BYTES;
         uint8_t* v_dst = sV + st * Cfg::V_BYTES;
+        mbar_arrive_expect_tx(&k_full[st], Cfg::K_BYTES);
 #pragma unroll
         for (int a = 0; a < Cfg::NA; ++a)
-          tma_load_3d(k_dst + a * Cfg::K_ATOM, &tmK, &kv_full[st], head * DH + a * Cfg::AW,
-                      j * KT, ring);
+          tma_load_3d(k_dst + a * Cfg::K_ATOM, &tmK, &k_full[st], head * DH + a * Cfg::AW, j * KT,
+                      ring);
+        mbar_arrive_expect_tx(&v_full[st], Cfg::V_BYTES);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(v_dst + a * Cfg::V_ATOM, &tmV, &kv_full[st], j * KT + a * 64, 0,
+          tma_load_3d(v_dst + a * Cfg::V_ATOM, &tmV, &v_full[st], j * KT + a * 64, 0,
                       ring * p.H + head);
         ++issued;
       }
       if (!ok || error_raised(p.err)) {
+        // Error path: let the loads already issued land before the CTA exits.
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(q_full, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
         }
         for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
-          while (!mbar_try_wait(&kv_full[j & 1], (j >> 1) & 1) &&
+          while (!mbar_try_wait(&k_full[j & 1], (j >> 1) & 1) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {
+          }
+          while (!mbar_try_wait(&v_full[j & 1], (j >> 1) & 1) &&
                  global_timer_ns() - t0 < kWaitLimitNs) {
           }
         }
@@ -150,159 +213,163 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------- MMA issuer
       constexpr uint32_t IDESC_S = umma_idesc_bf16(QT, KT);
       constexpr uint32_t IDESC_O = umma_idesc_bf16(QT, DH);
-      auto issue_s = [&](int j) {
-        const int st = j & 1;
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * Cfg::K_BYTES);
+      auto issue_s = [&](int i, int j) {
+        const uint32_t q0 = smem_u32(sQ + i * Cfg::Q_BYTES);
+        const uint32_t k0 = smem_u32(sK + (j & 1) * Cfg::K_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int e = kk * 16;
           const uint32_t off_q = (e / Cfg::AW) * Cfg::Q_ATOM + (e % Cfg::AW) * 2;
           const uint32_t off_k = (e / Cfg::AW) * Cfg::K_ATOM + (e % Cfg::AW) * 2;
-          umma_bf16(tmem + st * KT, umma_desc_kmajor(q0 + off_q, Cfg::ROWB),
+          umma_bf16(tmem + i * KT, umma_desc_kmajor(q0 + off_q, Cfg::ROWB),
                     umma_desc_kmajor(k0 + off_k, Cfg::ROWB), IDESC_S, kk != 0);
         }
-        umma_commit(&s_full[st]);
+        umma_commit(&s_full[i]);
       };
-      bool ok = mbar_wait(q_full, 0, p.err, ERR_ATTN_TIMEOUT);
-      if (ok) ok = mbar_wait(&kv_full[0], 0, p.err, ERR_ATTN_TIMEOUT);
+      auto issue_pv = [&](int i, int j) {
+        const uint32_t v0 = smem_u32(sV + (j & 1) * Cfg::V_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint32_t off_v = (kk >> 2) * Cfg::V_ATOM + (kk & 3) * 32;
+          umma_bf16_tmem_a(tmem + 2 * KT + i * 128, tmem + i * KT + kk * 8,
+                           umma_desc_kmajor(v0 + off_v, 128), IDESC_O, (j | kk) != 0);
+        }
+        umma_commit(&o_done[i]);
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, ERR_ATTN_TIMEOUT) &&
+                mbar_wait(&k_full[0], 0, p.err, ERR_ATTN_TIMEOUT);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        issue_s(0, 0);
+        if (has_q1) issue_s(1, 0);
       }
       for (int j = 0; j < nT && ok; ++j) {
-        if (j + 1 < nT) {
-          const int st1 = (j + 1) & 1;
-          const uint32_t use1 = (j + 1) >> 1;
-          if (!mbar_wait(&kv_full[st1], use1 & 1, p.err, ERR_ATTN_TIMEOUT) ||
-              !mbar_wait(&s_empty[st1], (use1 & 1) ^ 1, p.err, ERR_ATTN_TIMEOUT)) {
+        const int st = j & 1;
+        const bool next = j + 1 < nT;
+        if (!mbar_wait(&p_full[0], j & 1, p.err, ERR_ATTN_TIMEOUT) ||
+            !mbar_wait(&v_full[st], (j >> 1) & 1, p.err, ERR_ATTN_TIMEOUT)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, j);
+        if (next) {
+          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, p.err, ERR_ATTN_TIMEOUT)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(j + 1);
+          issue_s(0, j + 1);
         }
-        if (!mbar_wait(p_full, j & 1, p.err, ERR_ATTN_TIMEOUT)) {
-          ok = false;
-          break;
+        if (has_q1) {
+          if (!mbar_wait(&p_full[1], j & 1, p.err, ERR_ATTN_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(1, j);
+          if (next) issue_s(1, j + 1);
         }
-        tc_fence_after();
-        const uint32_t p0 = smem_u32(sP), v0 = smem_u32(sV + (j & 1) * Cfg::V_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint32_t off_p = (kk >> 2) * Cfg::P_ATOM + (kk & 3) * 32;
-          const uint32_t off_v = (kk >> 2) * Cfg::V_ATOM + (kk & 3) * 32;
-          umma_bf16(tmem_o, umma_desc_kmajor(p0 + off_p, 128), umma_desc_kmajor(v0 + off_v, 128),
-                    IDESC_O, (j | kk) != 0);
-        }
-        umma_commit(&kv_empty[j & 1]);
-        umma_commit(o_done);
+        umma_commit(&kv_empty[st]);
       }
     }
   } else {
-    // ---------------- softmax warps: thread = query row r of the tile
+    // ---------------- softmax warpgroups: thread = query row r of tile i
+    const int i = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.0f;
-    bool ok = true;
-    for (int j = 0; j < nT; ++j) {
-      const int st = j & 1;
-      if (!warp_wait(&s_full[st], (j >> 1) & 1, p.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[KT];
-#pragma unroll
-      for (int c = 0; c < KT / 32; ++c) tmem_ld32(tmem + st * KT + c * 32 + lane_off, s + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[st]);
-
-      const int key0 = j * KT;
-      if (key0 + KT > kv_len) {
-#pragma unroll
-        for (int c = 0; c < KT; ++c)
-          if (key0 + c >= kv_len) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < KT; ++c) mx = fmaxf(mx, s[c]);
-      const float m_tile = mx * sl2;
-
-      if (j > 0) {
-        if (!warp_wait(o_done, (j - 1) & 1, p.err)) {
+    if (i == 0 || has_q1) {
+      const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+      const uint32_t s_addr = tmem + i * KT + lane_off;
+      const uint32_t o_addr = tmem + 2 * KT + i * 128 + lane_off;
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY, l = 0.0f;
+      bool ok = true;
+      for (int j = 0; j < nT; ++j) {
+        if (!warp_wait(&s_full[i], j & 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      const bool grow = m_tile > m + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? m_tile : m;
-        const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
-        if (j > 0) {
-#pragma unroll 1
-          for (int c = 0; c < DH / 32; ++c) {
-            float o[32];
-            tmem_ld32(tmem_o + c * 32 + lane_off, o);
-            tmem_wait_ld();
+        float s[KT];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem_o + c * 32 + lane_off, o);
-          }
-          tmem_wait_st();
-        }
-        l *= alpha;
-        m = m_new;
-      }
-      // P = exp2(s * scale_log2 - m), row sum, bf16 into the swizzled tile.
-      float sum = 0.0f;
-      uint8_t* prow = sP + r * 128;
-#pragma unroll
-      for (int cidx = 0; cidx < KT / 8; ++cidx) {
-        float pv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          pv[i] = fast_exp2(fmaf(s[cidx * 8 + i], sl2, -m));
-          sum += pv[i];
-        }
-        uint4 w;
-        w.x = pack_bf16x2(pv[0], pv[1]);
-        w.y = pack_bf16x2(pv[2], pv[3]);
-        w.z = pack_bf16x2(pv[4], pv[5]);
-        w.w = pack_bf16x2(pv[6], pv[7]);
-        const int atom = cidx >> 3, chunk = cidx & 7;
-        *reinterpret_cast<uint4*>(prow + atom * Cfg::P_ATOM + ((chunk ^ (r & 7)) << 4)) = w;
-      }
-      l += sum;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && warp_wait(o_done, (nT - 1) & 1, p.err)) {
-      tc_fence_after();
-      const bool valid = (qt * QT + r) < p.T;
-      const float inv_l = 1.0f / l;
-      __nv_bfloat16* dst = p.o + static_cast<int64_t>(qrow0 + r) * p.d + head * DH;
-#pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
-        float o[32];
-        tmem_ld32(tmem_o + c * 32 + lane_off, o);
+        for (int c = 0; c < KT / 32; ++c) tmem_ld32(s_addr + c * 32, s + c * 32);
         tmem_wait_ld();
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        const int key0 = j * KT;
+        if (key0 + KT > kv_len) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(o[8 * i + 0] * inv_l, o[8 * i + 1] * inv_l);
-            w.y = pack_bf16x2(o[8 * i + 2] * inv_l, o[8 * i + 3] * inv_l);
-            w.z = pack_bf16x2(o[8 * i + 4] * inv_l, o[8 * i + 5] * inv_l);
-            w.w = pack_bf16x2(o[8 * i + 6] * inv_l, o[8 * i + 7] * inv_l);
-            d4[i] = w;
+          for (int c = 0; c < KT; ++c)
+            if (key0 + c >= kv_len) s[c] = -INFINITY;
+        }
+        float mx = max3(s[0], s[1], s[2]);
+#pragma unroll
+        for (int c = 3; c + 1 < KT; c += 2) mx = max3(mx, s[c], s[c + 1]);
+        mx = fmaxf(mx, s[KT - 1]);
+        const float m_tile = mx * sl2;
+        const bool grow = m_tile > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? m_tile : m;
+          const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
+          if (j > 0) {
+            // PV_{i,j-1} completed before S_{i,j} (in-order MMAs): O_i is stable.
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+              float o[32];
+              tmem_ld32(o_addr + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st32(o_addr + c * 32, o);
+            }
+          }
+          l *= alpha;
+          m = m_new;
+        }
+        // P = exp2(s * scale_log2 - m) in bf16, over the S columns just read.
+        const float negm = -m;
+        float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+        for (int c = 0; c < KT / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a = s[c * 32 + 2 * e], b = s[c * 32 + 2 * e + 1];
+            ffma2(a, b, sl2, negm);
+            a = fast_exp2(a);
+            b = fast_exp2(b);
+            fadd2(sum0, sum1, a, b);
+            pk[e] = pack_bf16x2(a, b);
+          }
+          tmem_st16(s_addr + c * 16, pk);
+        }
+        tmem_wait_st();
+        l += sum0 + sum1;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[i]);
+      }
+      if (ok && warp_wait(&o_done[i], (nT - 1) & 1, p.err)) {
+        tc_fence_after();
+        const bool valid = (pair * 2 * QT + i * QT + r) < p.T;
+        const float inv_l = 1.0f / l;
+        __nv_bfloat16* dst =
+            p.o + static_cast<int64_t>(qrow0 + i * QT + r) * p.d + head * DH;
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          float o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_wait_ld();
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16x2(o[8 * e + 0] * inv_l, o[8 * e + 1] * inv_l);
+              w.y = pack_bf16x2(o[8 * e + 2] * inv_l, o[8 * e + 3] * inv_l);
+              w.z = pack_bf16x2(o[8 * e + 4] * inv_l, o[8 * e + 5] * inv_l);
+              w.w = pack_bf16x2(o[8 * e + 6] * inv_l, o[8 * e + 7] * inv_l);
+              d4[e] = w;
+            }
           }
         }
       }
@@ -322,8 +389,6 @@ template <int DH>
 cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                       const AttnParams& p, int n_tasks, cudaStream_t st) {
   static bool attr_set = false;
-  // Every variant asks for more than half the SM's shared memory so that one
-  // CTA holds an SM: the 512 TMEM columns it allocates are then always free.
   const size_t smem = attn_smem_bytes(DH);
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<DH>,
@@ -332,8 +397,10 @@ cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUte
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int grid = n_tasks * p.H * p.n_qtiles;
-  attn_tc_kernel<DH><<<grid, 192, smem, st>>>(*tmQ, *tmK, *tmV, p);
+  AttnParams q = p;
+  q.n_qtiles = (p.T + 2 * QT - 1) / (2 * QT);  // query-tile pairs per (task, head)
+  const int grid = n_tasks * q.H * q.n_qtiles;
+  attn_tc_kernel<DH><<<grid, kThreads, smem, st>>>(*tmQ, *tmK, *tmV, q);
   return cudaGetLastError();
 }
 
@@ -346,6 +413,8 @@ size_t attn_smem_bytes(int dh) {
     case 64: need = AttnCfg<64>::SMEM; break;
     default: need = AttnCfg<128>::SMEM; break;
   }
+  // Every variant asks for more than half the SM's shared memory so that one
+  // CTA holds an SM: the 512 TMEM columns it allocates are then always free.
   const size_t one_per_sm = 120 * 1024;
   return need > one_per_sm ? need : one_per_sm;
 }

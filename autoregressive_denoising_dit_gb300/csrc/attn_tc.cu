@@ -22,6 +22,12 @@
 //               bf16 written to TMEM over its own S columns and consumed by
 //               the P.V MMA straight from TMEM.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+dh), O1 [384,..).
+// Long windows (>= 16 key tiles) are split into two fixed halves handled by
+// two CTAs, so that a wave's few hundred equal work units spread evenly over
+// the SMs; each half leaves its unnormalised O, m and l in a partial area and
+// the CTA that arrives second on the pair's counter merges both in a fixed
+// order (half 0, half 1), so the result does not depend on which finished
+// first.
 // tcgen05 MMAs of one issuing thread execute in order, so S_{i,j+1} (issued
 // after PV_{i,j}) only overwrites P_{i,j} once it was consumed, and when
 // S_{i,j+1} is complete O_i is stable for the softmax warps to rescale.
@@ -131,18 +137,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::N_BARS);
 
   const int warp = warp_id(), lane = lane_id();
-  // Full query pairs first, the task tails (one valid tile or less) last.
-  const int n_tasks = gridDim.x / (p.n_qtiles * p.H);
-  const int work = blockIdx.x;
-  const int ti = work % n_tasks;
-  const int head = (work / n_tasks) % p.H;
-  const int pair = work / (n_tasks * p.H);
+  __shared__ int s_last;
+  // Work item -> (task, head, query pair, key half).  Query pairs with two
+  // tiles come first, grouped by (task, head) so that CTAs sharing K/V run
+  // together; the task tails (pairs with a single tile) come last.
+  const int n_pairs = (p.T + 2 * QT - 1) / (2 * QT);
+  const int n_full = p.T > QT ? (p.T - QT + 2 * QT - 1) / (2 * QT) : 0;
+  int ti = 0, head = 0, pair = 0, half = 0, nsplit = 1;
+  {
+    int idx = blockIdx.x;
+    bool found = false;
+    for (int t = 0; t < p.n_tasks && !found; ++t) {
+      const int ns = ((p.tasks[t].kv_len + KT - 1) / KT >= kAttnSplitMinTiles) ? 2 : 1;
+      const int cnt = p.H * n_full * ns;
+      if (idx < cnt) {
+        ti = t, nsplit = ns, half = idx % ns, pair = (idx / ns) % n_full, head = idx / (ns * n_full);
+        found = true;
+      } else {
+        idx -= cnt;
+      }
+    }
+    for (int t = 0; t < p.n_tasks && !found; ++t) {
+      const int ns = ((p.tasks[t].kv_len + KT - 1) / KT >= kAttnSplitMinTiles) ? 2 : 1;
+      const int cnt = p.H * (n_pairs - n_full) * ns;
+      if (idx < cnt) {
+        ti = t, nsplit = ns, half = idx % ns, pair = n_full, head = idx / ns;
+        found = true;
+      } else {
+        idx -= cnt;
+      }
+    }
+  }
   const TaskDev task = p.tasks[ti];
   const int ring = task.ring0 + p.block * p.S;
   const int kv_len = task.kv_len;
-  const int nT = (kv_len + KT - 1) / KT;
+  const int nT_all = (kv_len + KT - 1) / KT;
+  const int j_begin = (half == 0) ? 0 : nT_all / 2;
+  const int j_end = (nsplit == 1 || half == 1) ? nT_all : nT_all / 2;
+  const int nT = j_end - j_begin;  // key tiles of this CTA: [j_begin, j_end)
   const int qrow0 = task.row0 + pair * 2 * QT;  // first query row in the wave batch
   const bool has_q1 = pair * 2 * QT + QT < p.T;
+  const int item = (ti * p.H + head) * p.max_pairs + pair;
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 4 : 1);
@@ -184,12 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], Cfg::K_BYTES);
 #pragma unroll
         for (int a = 0; a < Cfg::NA; ++a)
-          tma_load_3d(k_dst + a * Cfg::K_ATOM, &tmK, &k_full[st], head * DH + a * Cfg::AW, j * KT,
-                      ring);
+          tma_load_3d(k_dst + a * Cfg::K_ATOM, &tmK, &k_full[st], head * DH + a * Cfg::AW,
+                      (j_begin + j) * KT, ring);
         mbar_arrive_expect_tx(&v_full[st], Cfg::V_BYTES);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
-          tma_load_3d(v_dst + a * Cfg::V_ATOM, &tmV, &v_full[st], j * KT + a * 64, 0,
+          tma_load_3d(v_dst + a * Cfg::V_ATOM, &tmV, &v_full[st], (j_begin + j) * KT + a * 64, 0,
                       ring * p.H + head);
         ++issued;
       }
@@ -278,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    if (i == 0 || has_q1) {
-      const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-      const uint32_t s_addr = tmem + i * KT + lane_off;
-      const uint32_t o_addr = tmem + 2 * KT + i * 128 + lane_off;
+    const bool active = (i == 0 || has_q1);
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t s_addr = tmem + i * KT + lane_off;
+    const uint32_t o_addr = tmem + 2 * KT + i * 128 + lane_off;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    if (active) {
       const float sl2 = p.scale_log2;
-      float m = -INFINITY, l = 0.0f;
-      bool ok = true;
       for (int j = 0; j < nT; ++j) {
         if (!warp_wait(&s_full[i], j & 1, p.err)) {
           ok = false;
@@ -295,16 +331,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < KT / 32; ++c) tmem_ld32(s_addr + c * 32, s + c * 32);
         tmem_wait_ld();
-        const int key0 = j * KT;
+        const int key0 = (j_begin + j) * KT;
         if (key0 + KT > kv_len) {
 #pragma unroll
           for (int c = 0; c < KT; ++c)
             if (key0 + c >= kv_len) s[c] = -INFINITY;
         }
-        float mx = max3(s[0], s[1], s[2]);
+        // row max: 8 independent chains, then a tree
+        float mx8[8];
 #pragma unroll
-        for (int c = 3; c + 1 < KT; c += 2) mx = max3(mx, s[c], s[c + 1]);
-        mx = fmaxf(mx, s[KT - 1]);
+        for (int c = 0; c < 8; ++c) mx8[c] = max3(s[c], s[c + 8], s[c + 16]);
+#pragma unroll
+        for (int c = 24; c < KT; c += 16) {
+          if (c + 16 <= KT) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = max3(mx8[e], s[c + e], s[c + 8 + e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+          }
+        }
+        const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                               fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_tile = mx * sl2;
         const bool grow = m_tile > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, grow)) {
@@ -325,9 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m = m_new;
         }
-        // P = exp2(s * scale_log2 - m) in bf16, over the S columns just read.
+        // P = exp2(s * scale_log2 - m) in bf16, over the S columns just read;
+        // row sum in 4 independent packed accumulators.
         const float negm = -m;
-        float sum0 = 0.0f, sum1 = 0.0f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < KT / 32; ++c) {
           uint32_t pk[16];
@@ -337,41 +386,90 @@ __global__ void __launch_bounds__(kThreads, 1)
             ffma2(a, b, sl2, negm);
             a = fast_exp2(a);
             b = fast_exp2(b);
-            fadd2(sum0, sum1, a, b);
+            fadd2(acc[2 * (e & 3)], acc[2 * (e & 3) + 1], a, b);
             pk[e] = pack_bf16x2(a, b);
           }
           tmem_st16(s_addr + c * 16, pk);
         }
         tmem_wait_st();
-        l += sum0 + sum1;
+        l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[i]);
       }
-      if (ok && warp_wait(&o_done[i], (nT - 1) & 1, p.err)) {
-        tc_fence_after();
-        const bool valid = (pair * 2 * QT + i * QT + r) < p.T;
+      if (ok) ok = warp_wait(&o_done[i], (nT - 1) & 1, p.err);
+      if (ok) tc_fence_after();
+    }
+    const bool valid = active && (pair * 2 * QT + i * QT + r) < p.T;
+    __nv_bfloat16* dst = p.o + static_cast<int64_t>(qrow0 + i * QT + r) * p.d + head * DH;
+    auto store_row = [&](const float* o, int c, float inv) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
+        w.y = pack_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
+        w.z = pack_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
+        w.w = pack_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
+        d4[e] = w;
+      }
+    };
+    if (nsplit == 1) {
+      if (active && ok) {
         const float inv_l = 1.0f / l;
-        __nv_bfloat16* dst =
-            p.o + static_cast<int64_t>(qrow0 + i * QT + r) * p.d + head * DH;
 #pragma unroll 1
         for (int c = 0; c < DH / 32; ++c) {
           float o[32];
           tmem_ld32(o_addr + c * 32, o);
           tmem_wait_ld();
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          if (valid) store_row(o, c, inv_l);
+        }
+      }
+    } else {
+      // Leave this half's unnormalised O, m, l; the second CTA of the pair to
+      // arrive merges both halves.
+      constexpr int PART = (DH + 2) * QT;
+      float* base = p.part + static_cast<int64_t>(item) * 4 * PART;
+      float* mine = base + (half * 2 + i) * PART;
+      const float* other = base + ((1 - half) * 2 + i) * PART;
+      if (active && ok) {
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          float o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint4 w;
-              w.x = pack_bf16x2(o[8 * e + 0] * inv_l, o[8 * e + 1] * inv_l);
-              w.y = pack_bf16x2(o[8 * e + 2] * inv_l, o[8 * e + 3] * inv_l);
-              w.z = pack_bf16x2(o[8 * e + 4] * inv_l, o[8 * e + 5] * inv_l);
-              w.w = pack_bf16x2(o[8 * e + 6] * inv_l, o[8 * e + 7] * inv_l);
-              d4[e] = w;
+          for (int e = 0; e < 32; ++e) mine[(c * 32 + e) * QT + r] = o[e];
+        }
+        mine[DH * QT + r] = m;
+        mine[(DH + 1) * QT + r] = l;
+      }
+      __threadfence();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (warp == 2 && lane == 0) s_last = (ok && !error_raised(p.err)) ? atomicAdd(&p.counters[item], 1) : -1;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (s_last == 1) {
+        __threadfence();
+        if (active) {
+          const float* h0 = half == 0 ? mine : other;
+          const float* h1 = half == 0 ? other : mine;
+          const float m0 = __ldcg(h0 + DH * QT + r), m1 = __ldcg(h1 + DH * QT + r);
+          const float l0 = __ldcg(h0 + (DH + 1) * QT + r), l1 = __ldcg(h1 + (DH + 1) * QT + r);
+          const float mm = fmaxf(m0, m1);
+          const float a0 = fast_exp2(m0 - mm), a1 = fast_exp2(m1 - mm);
+          const float inv = 1.0f / (l0 * a0 + l1 * a1);
+#pragma unroll 1
+          for (int c = 0; c < DH / 32; ++c) {
+            float o[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int k = (c * 32 + e) * QT + r;
+              o[e] = __ldcg(h0 + k) * a0 + __ldcg(h1 + k) * a1;
             }
+            if (valid) store_row(o, c, inv);
           }
         }
+        if (warp == 2 && lane == 0) p.counters[item] = 0;
       }
     }
   }
@@ -387,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DH>
 cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                      const AttnParams& p, int n_tasks, cudaStream_t st) {
+                      const AttnParams& p, int n_tasks, int grid, cudaStream_t st) {
   static bool attr_set = false;
   const size_t smem = attn_smem_bytes(DH);
   if (!attr_set) {
@@ -398,8 +496,7 @@ cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUte
     attr_set = true;
   }
   AttnParams q = p;
-  q.n_qtiles = (p.T + 2 * QT - 1) / (2 * QT);  // query-tile pairs per (task, head)
-  const int grid = n_tasks * q.H * q.n_qtiles;
+  q.n_tasks = n_tasks;
   attn_tc_kernel<DH><<<grid, kThreads, smem, st>>>(*tmQ, *tmK, *tmV, q);
   return cudaGetLastError();
 }
@@ -420,14 +517,30 @@ size_t attn_smem_bytes(int dh) {
 }
 
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                             const CUtensorMap* tmV, const AttnParams& p, int n_tasks,
+                             const CUtensorMap* tmV, const AttnParams& p, int n_tasks, int grid,
                              cudaStream_t st) {
+  if (grid <= 0) return cudaSuccess;
   switch (p.dh) {
-    case 32: return launch_dh<32>(tmQ, tmK, tmV, p, n_tasks, st);
-    case 64: return launch_dh<64>(tmQ, tmK, tmV, p, n_tasks, st);
-    case 128: return launch_dh<128>(tmQ, tmK, tmV, p, n_tasks, st);
+    case 32: return launch_dh<32>(tmQ, tmK, tmV, p, n_tasks, grid, st);
+    case 64: return launch_dh<64>(tmQ, tmK, tmV, p, n_tasks, grid, st);
+    case 128: return launch_dh<128>(tmQ, tmK, tmV, p, n_tasks, grid, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H) {
+  const int n_pairs = (T + 2 * QT - 1) / (2 * QT);
+  int total = 0;
+  for (int t = 0; t < n_tasks; ++t) {
+    const int ns = ((kv_lens[t] + KT - 1) / KT >= kAttnSplitMinTiles) ? 2 : 1;
+    total += H * n_pairs * ns;
+  }
+  return total;
+}
+
+size_t attn_part_floats(int max_tasks, int T, int H, int dh) {
+  const int n_pairs = (T + 2 * QT - 1) / (2 * QT);
+  return static_cast<size_t>(max_tasks) * H * n_pairs * 4 * (dh + 2) * QT;
 }
 
 }  // namespace psv

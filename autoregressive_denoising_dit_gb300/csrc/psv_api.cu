@@ -55,6 +55,8 @@ struct Layout {
   size_t k_ring, vt_ring, rings_end;
   size_t h, y, q, o, u, acts_end;
   size_t state, mod, fmod, rope_local, rope_base, tasks, err, scratch;
+  size_t attn_part, attn_cnt;  // split-KV partials and arrival counters
+  int attn_pairs;
   size_t total;
 };
 
@@ -145,6 +147,9 @@ Layout plan_layout(const psv_model_desc& m) {
   L.tasks = take(static_cast<size_t>(L.max_tasks) * sizeof(TaskDev));
   L.err = take(256);
   L.scratch = take(static_cast<size_t>(8) * (m.t_embed + 3 * d) * 4 + d * 4);
+  L.attn_pairs = (m.T + 255) / 256;
+  L.attn_part = take(psv::attn_part_floats(L.max_tasks, m.T, m.H, m.dh) * 4);
+  L.attn_cnt = take(static_cast<size_t>(L.max_tasks) * m.H * L.attn_pairs * 4);
   L.total = off;
   return L;
 }
@@ -240,8 +245,8 @@ struct psv_ctx {
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
   // executor
   bool use_graphs = true;
-  std::map<int, int> shape_seen;
-  std::map<int, cudaGraphExec_t> graphs;
+  std::map<int64_t, int> shape_seen;
+  std::map<int64_t, cudaGraphExec_t> graphs;
   bool profiling = false;
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> ev_pool;
@@ -418,12 +423,13 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
   });
 
   double attn_flops = 0.0, attn_bytes = 0.0;
-  if (host_tasks) {
-    for (const TaskDev& t : *host_tasks) {
-      attn_flops += 4.0 * m.T * static_cast<double>(t.kv_len) * d;
-      attn_bytes += (2.0 * m.T * d + 2.0 * static_cast<double>(t.kv_len) * d) * 2.0;
-    }
+  std::vector<int> kv_lens;
+  for (const TaskDev& t : *host_tasks) {
+    attn_flops += 4.0 * m.T * static_cast<double>(t.kv_len) * d;
+    attn_bytes += (2.0 * m.T * d + 2.0 * static_cast<double>(t.kv_len) * d) * 2.0;
+    kv_lens.push_back(t.kv_len);
   }
+  const int attn_grid = psv::attn_grid_size(kv_lens.data(), n, m.T, m.H);
 
   for (int b = 0; b < m.B; ++b) {
     if (tap && b == ctx->tap_block && run.err == cudaSuccess)
@@ -461,13 +467,16 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       a.Lr = L.Lr;
       a.Lp = L.Lp;
       a.block = b;
-      a.n_qtiles = (m.T + 127) / 128;
+      a.n_tasks = n;
       a.tasks = tasks;
       a.o = ctx->at<__nv_bfloat16>(L.o);
       a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m.dh)));
+      a.part = ctx->at<float>(L.attn_part);
+      a.counters = ctx->at<int>(L.attn_cnt);
+      a.max_pairs = L.attn_pairs;
       a.err = ctx->at<int>(L.err);
       run.run(K_ATTN, attn_flops, attn_bytes, [&] {
-        return psv::launch_attention(&ctx->tmQ, &ctx->tmK, &ctx->tmV, a, n, st);
+        return psv::launch_attention(&ctx->tmQ, &ctx->tmK, &ctx->tmV, a, n, attn_grid, st);
       });
     }
     // out-proj + gated residual (gate1)
@@ -956,8 +965,14 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
       CK(enqueue_wave(ctx, ctx->stream, n, ctx->profiling, tap, &dev), "wave launch");
       ctx->tap_block = -1;
     } else {
-      int& seen = ctx->shape_seen[n];
-      auto it = ctx->graphs.find(n);
+      // A wave's launches depend on its task count and on how many attention
+      // CTAs its windows need (fill waves have shorter windows).
+      std::vector<int> kvl;
+      for (const TaskDev& t : dev) kvl.push_back(t.kv_len);
+      const int64_t key = (static_cast<int64_t>(n) << 32) |
+                          static_cast<int64_t>(psv::attn_grid_size(kvl.data(), n, ctx->m.T, ctx->m.H));
+      int& seen = ctx->shape_seen[key];
+      auto it = ctx->graphs.find(key);
       if (it == ctx->graphs.end() && seen >= 1) {
         // Captured on a private stream (capture is not allowed on the legacy
         // default stream a caller may pass); replayed on the caller's stream.
@@ -971,7 +986,7 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
         cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
         cudaGraphDestroy(g);
         if (ie != cudaSuccess) return cuda_fail(ctx, ie, "graph instantiate");
-        it = ctx->graphs.emplace(n, ex).first;
+        it = ctx->graphs.emplace(key, ex).first;
       }
       if (it != ctx->graphs.end()) {
         CK(cudaGraphLaunch(it->second, ctx->stream), "graph launch");

@@ -47,12 +47,25 @@ struct GemmParams {
 struct AttnParams {
   int T, d, dh, H, S, Lr, Lp;
   int block;
-  int n_qtiles;            // ceil(T / 128)
+  int n_tasks;
   const TaskDev* tasks;
   __nv_bfloat16* o;        // [rows][d]
   float scale_log2;        // log2(e) / sqrt(dh)
+  // Split-KV partials: per (task, head, query pair) 2 halves x 2 query tiles
+  // of [dh + 2][128] f32 (O transposed, then m, l), and one arrival counter.
+  float* part;
+  int* counters;
+  int max_pairs;           // query pairs per (task, head) the partial area is sized for
   int* err;
 };
+
+// Key tiles (of 128) from which a (task, head, query pair) is split in two
+// halves processed by two CTAs; depends on the task's kv_len only, so the
+// result of a task does not depend on the rest of the wave.
+constexpr int kAttnSplitMinTiles = 16;
+// CTAs an attention launch over these kv lengths needs.
+int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H);
+size_t attn_part_floats(int max_tasks, int T, int H, int dh);
 
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 4;
 size_t gemm_smem_bytes();
@@ -61,7 +74,7 @@ size_t attn_smem_bytes(int dh);
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                             const CUtensorMap* tmV, const AttnParams& p, int n_tasks,
+                             const CUtensorMap* tmV, const AttnParams& p, int n_tasks, int grid,
                              cudaStream_t st);
 
 // Memory-bound kernels.

@@ -152,3 +152,19 @@ def test_staggered_submission_and_polling_match_oracle():
     assert sorted(got) == list(range(6))
     for c in range(6):
         assert rel_l2(got[c], ora[c]) <= TOL_FINAL
+
+
+def test_long_window_split_kv_matches_oracle():
+    """W = 10, T = 200: windows of up to 2200 keys (18 tiles of 128, the last
+    ragged) are split across two CTAs per query pair and merged; the result
+    must match the oracle and stay batch invariant."""
+    cfg = synth.config("mid", W=10, n_chunks=13)
+    w = synth.make_weights(cfg, 0)
+    streams = synth.make_streams(cfg)
+    gpu, ora = _compare(cfg, w, streams, 13)
+    from autoregressive_denoising_dit_gb300 import _psv as P
+
+    seq, _ = run_gpu(cfg, w, streams, 13, flags=P.PSV_FLAG_SEQUENTIAL)
+    for i in range(2):
+        for c in range(13):
+            np.testing.assert_array_equal(gpu[i][c], seq[i][c])

@@ -44,7 +44,7 @@ EXPORTS = [
     "psv_submit_chunk", "psv_run_wave", "psv_poll_chunk", "psv_sync",
     "psv_wave_plan", "psv_close_stream", "psv_destroy", "psv_last_error",
     "psv_set_graphs", "psv_set_profiling", "psv_kernel_times", "psv_debug_tap",
-    "psv_debug_read_kv",
+    "psv_debug_read_kv", "psv_attention_scratch_bytes", "psv_attention",
 ]
 
 
@@ -72,6 +72,10 @@ class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64),
                 ("total_ms", ctypes.c_double), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double)]
+
+
+class AttnProblem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n", "T", "H", "dh", "L", "k_rows", "vt_cols")]
 
 
 class PSVError(RuntimeError):
@@ -110,6 +114,8 @@ def lib() -> ctypes.CDLL:
             "psv_kernel_times": (i32, [vp, ctypes.POINTER(KernelTime), i32, ctypes.POINTER(i32)]),
             "psv_debug_tap": (i32, [vp, i32, vp, vp]),
             "psv_debug_read_kv": (i32, [vp, i32, i32, i32, vp, vp]),
+            "psv_attention_scratch_bytes": (i32, [ctypes.POINTER(AttnProblem), ctypes.POINTER(sz)]),
+            "psv_attention": (i32, [ctypes.POINTER(AttnProblem), vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -257,3 +263,19 @@ def psv_debug_read_kv(ctx, sid: int, block: int, step: int, rows: int, d: int):
     v = np.empty((rows, d), dtype=np.float32)
     _check(ctx, lib().psv_debug_read_kv(ctx, sid, block, step, _fptr(k), _fptr(v)))
     return k, v
+
+
+def psv_attention_scratch_bytes(prob: AttnProblem) -> int:
+    n = ctypes.c_size_t()
+    _check(None, lib().psv_attention_scratch_bytes(ctypes.byref(prob), ctypes.byref(n)))
+    return n.value
+
+
+def psv_attention(prob: AttnProblem, q_ptr: int, k_ptr: int, vt_ptr: int, o_ptr: int,
+                  scratch_ptr: int, scratch_bytes: int, stream_ptr: int = 0) -> None:
+    r = lib().psv_attention(ctypes.byref(prob), ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr),
+                            ctypes.c_void_p(vt_ptr), ctypes.c_void_p(o_ptr),
+                            ctypes.c_void_p(scratch_ptr), scratch_bytes,
+                            ctypes.c_void_p(stream_ptr or None))
+    if r < 0:
+        raise PSVError(r, "psv_attention rejected its arguments")

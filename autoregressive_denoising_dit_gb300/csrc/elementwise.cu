@@ -7,30 +7,25 @@ namespace psv {
 
 namespace {
 
-constexpr int LN_THREADS = 128;
-constexpr int LN_MAXV = 12;  // float4 per thread: d <= 12 * 4 * 128 = 6144
+constexpr int LN_WARPS = 8;  // rows per CTA (one warp per row)
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  float t = 0.0f;
-#pragma unroll
-  for (int i = 0; i < LN_THREADS / 32; ++i) t += red[i];
-  return t;
+  return v;
 }
 
-// One row per CTA; the row stays in registers between the two passes
-// (mean, then centred second moment), so h is read from HBM once.
-__global__ void __launch_bounds__(LN_THREADS)
-    ln_mod_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int d, int T,
+// One warp per row; the row stays in registers (MAXV float4 per lane, d up
+// to 128 * MAXV) between the two passes (mean, then centred second moment),
+// so h is read once and no block-wide synchronisation is needed.
+template <int MAXV>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_mod_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int M, int d, int T,
                   const TaskDev* __restrict__ tasks, const float* __restrict__ table,
                   int use_fmod, int block, int shift_off, int scale_off, float eps) {
-  __shared__ float red[LN_THREADS / 32];
-  const int row = blockIdx.x;
+  const int row = blockIdx.x * LN_WARPS + warp_id();
+  if (row >= M) return;
+  const int lane = lane_id();
   const TaskDev& t = tasks[row / T];
   const float* base = table + (use_fmod ? static_cast<int64_t>(t.fmod0)
                                         : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
@@ -39,31 +34,31 @@ __global__ void __launch_bounds__(LN_THREADS)
   const float4* hr = reinterpret_cast<const float4*>(h + static_cast<int64_t>(row) * d);
   const int nv = d >> 2;
 
-  float4 v[LN_MAXV];
+  float4 v[MAXV];
   float s = 0.0f;
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
-    const int k = threadIdx.x + i * LN_THREADS;
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = lane + i * 32;
     if (k < nv) {
-      v[i] = hr[k];
+      v[i] = __ldg(hr + k);
       s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
     }
   }
-  const float mean = block_sum(s, red) / static_cast<float>(d);
+  const float mean = warp_sum(s) / static_cast<float>(d);
   float q = 0.0f;
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
-    const int k = threadIdx.x + i * LN_THREADS;
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = lane + i * 32;
     if (k < nv) {
       const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
       q += (a * a + b * b) + (c * c + e * e);
     }
   }
-  const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(d) + eps);
+  const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(d) + eps);
   uint2* yr = reinterpret_cast<uint2*>(y + static_cast<int64_t>(row) * d);
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
-    const int k = threadIdx.x + i * LN_THREADS;
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = lane + i * 32;
     if (k < nv) {
       const float4 sh = __ldg(shift + k), sc = __ldg(scale + k);
       uint2 o;
@@ -84,7 +79,7 @@ __global__ void __launch_bounds__(IP_COLS)
                    const float* __restrict__ b_in, float* __restrict__ h, int M, int d, int C,
                    int T, const TaskDev* __restrict__ tasks) {
   __shared__ float xs[IP_ROWS][IP_KC + 1];
-  __shared__ float ws[IP_KC][IP_COLS];
+  __shared__ float ws[IP_KC][IP_COLS + 1];
   const int r0 = blockIdx.x * IP_ROWS;
   const int n = blockIdx.y * IP_COLS + threadIdx.x;
   float acc[IP_ROWS];
@@ -102,7 +97,7 @@ __global__ void __launch_bounds__(IP_COLS)
       xs[rr][kk] = xv;
     }
     for (int idx = threadIdx.x; idx < IP_KC * IP_COLS; idx += IP_COLS) {
-      const int kk = idx / IP_COLS, nn = idx % IP_COLS;
+      const int nn = idx / IP_KC, kk = idx % IP_KC;  // k fastest: coalesced weight rows
       const int col = blockIdx.y * IP_COLS + nn, k = k0 + kk;
       ws[kk][nn] = (col < d && k < C)
                        ? __bfloat162float(w_in[static_cast<int64_t>(col) * C + k])
@@ -190,9 +185,24 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
                           const TaskDev* tasks, const float* table, int use_fmod, int block,
                           int shift_off, int scale_off, float eps, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  if (d % 4 != 0 || d > LN_MAXV * 4 * LN_THREADS) return cudaErrorInvalidValue;
-  ln_mod_kernel<<<M, LN_THREADS, 0, st>>>(h, y, d, T, tasks, table, use_fmod, block, shift_off,
-                                          scale_off, eps);
+  if (d % 4 != 0) return cudaErrorInvalidValue;
+  const int nv = d / 4;
+  const int grid = (M + LN_WARPS - 1) / LN_WARPS;
+#define PSV_LN_LAUNCH(V)                                                                     \
+  ln_mod_kernel<V><<<grid, LN_WARPS * 32, 0, st>>>(h, y, M, d, T, tasks, table, use_fmod, \
+                                                   block, shift_off, scale_off, eps)
+  if (nv <= 32 * 1) PSV_LN_LAUNCH(1);
+  else if (nv <= 32 * 2) PSV_LN_LAUNCH(2);
+  else if (nv <= 32 * 4) PSV_LN_LAUNCH(4);
+  else if (nv <= 32 * 8) PSV_LN_LAUNCH(8);
+  else if (nv <= 32 * 12) PSV_LN_LAUNCH(12);
+  else if (nv <= 32 * 16) PSV_LN_LAUNCH(16);
+  else if (nv <= 32 * 24) PSV_LN_LAUNCH(24);
+  else if (nv <= 32 * 32) PSV_LN_LAUNCH(32);
+  else if (nv <= 32 * 40) PSV_LN_LAUNCH(40);
+  else if (nv <= 32 * 48) PSV_LN_LAUNCH(48);
+  else return cudaErrorInvalidValue;
+#undef PSV_LN_LAUNCH
   return cudaGetLastError();
 }
 

@@ -167,9 +167,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// bf16 tensor map: dims innermost first, strides in bytes for dims 1..rank-1.
-bool encode_bf16(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
-                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+}  // namespace
+
+bool psv::encode_bf16_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint32_t es[3] = {1, 1, 1};
@@ -177,6 +178,13 @@ bool encode_bf16(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool encode_bf16(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  return psv::encode_bf16_map(map, rank, base, dims, strides, box, sw);
 }
 
 uint16_t f32_to_bf16_bits(float f) {

@@ -92,5 +92,13 @@ cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat1
                                const float* b, const float* add, float* out, int N,
                                int silu_in, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, cudaStream_t st);
+// Task table of a standalone attention call: block i = rows [i*T, i*T+T),
+// keys of "ring" i, kv_len = L.
+cudaError_t launch_fill_attn_tasks(TaskDev* tasks, int n, int T, int L, cudaStream_t st);
+
+// bf16 tiled tensor map (dims innermost first, strides in bytes for dims
+// 1..rank-1); false if the driver entry point or the arguments are rejected.
+bool encode_bf16_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
 
 }  // namespace psv

@@ -209,6 +209,31 @@ int psv_debug_tap(psv_ctx* ctx, int block, float* h_in, float* h_out);
 int psv_debug_read_kv(psv_ctx* ctx, int stream_id, int block, int step,
                       float* k, float* v);
 
+/* ---- kernel-level window attention ---------------------------------------
+ * The attention step of the wave (AREX article "vLLM 与 Physis-AI 联合介绍
+ * PhysisServe 推理系统", §难题: a chunk's queries attend to its own keys and
+ * the still-noisy keys the preceding chunks left) as a standalone call on
+ * caller buffers: n independent query blocks; the T queries of block i
+ * attend to the L keys of block i with softmax scale 1/sqrt(dh), no mask.
+ *   q   bf16 [n*T][H*dh]            row-major; head h = columns [h*dh, (h+1)*dh)
+ *   k   bf16 [n][k_rows][H*dh]      keys of block i at rows [0, L)
+ *   vt  bf16 [n][H][dh][vt_cols]    values transposed per head, keys at cols [0, L)
+ *   o   bf16 [n*T][H*dh]            output (written)
+ * Requirements: dh in {32, 64, 128}; H*dh % 8 == 0; 1 <= L <= k_rows;
+ * L <= vt_cols, vt_cols % 8 == 0; all pointers 16-byte aligned device memory.
+ * scratch: caller-owned device memory of at least psv_attention_scratch_bytes
+ * bytes (task table, split-key partials, arrival counters), 256-byte aligned;
+ * it is overwritten and must not be shared by calls that may overlap on the
+ * GPU.  Asynchronous on cuda_stream; the int at the start of scratch is set
+ * nonzero if a device-side pipeline wait timed out.  Errors: PSV_EINVAL. */
+typedef struct psv_attn_problem {
+  int32_t n, T, H, dh, L, k_rows, vt_cols;
+} psv_attn_problem;
+
+int psv_attention_scratch_bytes(const psv_attn_problem* p, size_t* bytes);
+int psv_attention(const psv_attn_problem* p, const void* q, const void* k, const void* vt,
+                  void* o, void* scratch, size_t scratch_bytes, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -45,7 +45,10 @@ EXPORTS = [
     "psv_wave_plan", "psv_close_stream", "psv_destroy", "psv_last_error",
     "psv_set_graphs", "psv_set_profiling", "psv_kernel_times", "psv_debug_tap",
     "psv_debug_read_kv", "psv_attention_scratch_bytes", "psv_attention",
+    "psv_attention_noalloc",
 ]
+
+PSV_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class ModelDesc(ctypes.Structure):
@@ -116,6 +119,7 @@ def lib() -> ctypes.CDLL:
             "psv_debug_read_kv": (i32, [vp, i32, i32, i32, vp, vp]),
             "psv_attention_scratch_bytes": (i32, [ctypes.POINTER(AttnProblem), ctypes.POINTER(sz)]),
             "psv_attention": (i32, [ctypes.POINTER(AttnProblem), vp, vp, vp, vp, vp, sz, vp]),
+            "psv_attention_noalloc": (i32, [ctypes.POINTER(AttnProblem), vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -279,3 +283,16 @@ def psv_attention(prob: AttnProblem, q_ptr: int, k_ptr: int, vt_ptr: int, o_ptr:
                             ctypes.c_void_p(stream_ptr or None))
     if r < 0:
         raise PSVError(r, "psv_attention rejected its arguments")
+
+
+def psv_attention_noalloc(prob: AttnProblem, q_ptr: int, k_ptr: int, vt_ptr: int, o_ptr: int,
+                          stream_ptr: int = 0) -> None:
+    """psv_attention with the library's fixed scratch array (no allocation)."""
+    r = lib().psv_attention_noalloc(ctypes.byref(prob), ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr),
+                                    ctypes.c_void_p(vt_ptr), ctypes.c_void_p(o_ptr),
+                                    ctypes.c_void_p(stream_ptr or None))
+    if r == PSV_ENOMEM:
+        raise PSVError(r, "psv_attention_noalloc: the problem needs more scratch than the "
+                          f"fixed {PSV_ATTN_NOALLOC_SCRATCH_BYTES >> 20} MiB array holds")
+    if r < 0:
+        raise PSVError(r, "psv_attention_noalloc rejected its arguments (shape or alignment)")

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/psv.h"
@@ -131,4 +132,46 @@ PSV_API int psv_attention(const psv_attn_problem* p, const void* q, const void* 
   if (scratch_bytes < attn_scratch_layout(*p).total) return PSV_EINVAL;
   return psv_attention_enqueue(p, q, k, vt, o, static_cast<char*>(scratch),
                                static_cast<cudaStream_t>(cuda_stream));
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot allocate device memory when
+// they call: a control loop that must never enter the CUDA allocator after
+// start-up (its latency and failure modes are not bounded), or a host
+// framework that owns every device allocation and hands out no scratch.  For
+// them the scratch of the attention call lives in this file-scope array,
+// which the CUDA module reserves once per device when the library is loaded
+// and keeps until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = PSV_ATTN_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+char* g_scratch_ptr[64] = {};  // device address of g_attn_scratch, per device
+
+}  // namespace
+
+PSV_API int psv_attention_noalloc(const psv_attn_problem* p, const void* q, const void* k,
+                                  const void* vt, void* o, void* cuda_stream) {
+  if (!attn_problem_ok(p)) return PSV_EINVAL;
+  if (!q || !k || !vt || !o) return PSV_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o)) return PSV_EINVAL;
+  if (attn_scratch_layout(*p).total > kNoAllocScratchBytes) return PSV_ENOMEM;  // over the fixed size
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PSV_ECUDA;
+  char* scratch = nullptr;
+  {
+    // Set-up on the first call on each device, with that device current: the
+    // host-side name g_attn_scratch is only a stand-in, the kernel needs the
+    // device address.
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) return PSV_ECUDA;
+      g_scratch_ptr[dev] = static_cast<char*>(ptr);
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  return psv_attention_enqueue(p, q, k, vt, o, scratch, static_cast<cudaStream_t>(cuda_stream));
 }

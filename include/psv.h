@@ -234,6 +234,27 @@ int psv_attention_scratch_bytes(const psv_attn_problem* p, size_t* bytes);
 int psv_attention(const psv_attn_problem* p, const void* q, const void* k, const void* vt,
                   void* o, void* scratch, size_t scratch_bytes, void* cuda_stream);
 
+/* Allocation-free psv_attention (the pages have no counterpart: this is a
+ * deployment convenience).  For callers that cannot allocate device memory
+ * at call time, e.g. a real-time control loop that must not enter the CUDA
+ * allocator after start-up, or a host framework that owns all device memory
+ * and provides no scratch.  Same arguments and results as psv_attention,
+ * without scratch: the library uses a fixed array of
+ * PSV_ATTN_NOALLOC_SCRATCH_BYTES bytes that the CUDA module reserves on every
+ * device that loads libpsv and keeps until the process exits.  Problems
+ * whose scratch (psv_attention_scratch_bytes) exceeds that size are rejected
+ * with PSV_ENOMEM; bad shapes or pointers with PSV_EINVAL.  The call
+ * allocates nothing.  Its first call on a device
+ * looks up the array's device address (with that device current), so make
+ * that first call before any stream capture.  Every call shares the one
+ * array (the call clears the parts that must start at zero); calls whose
+ * work may overlap on the GPU race on it and must be ordered by the caller
+ * (e.g. issued on one stream).  Device-side pipeline timeouts are recorded
+ * in the shared array, not returned. */
+#define PSV_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int psv_attention_noalloc(const psv_attn_problem* p, const void* q, const void* k,
+                          const void* vt, void* o, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,8 +5,9 @@
 // tcgen05.mma directly.  One CTA per SM, warp-specialised:
 //   warp 0      TMA producer (4-stage smem ring, 48 KB per stage)
 //   warp 1      TMEM allocator + single-thread MMA issuer (128x256x16 MMAs)
-//   warps 2..5  epilogue: tcgen05.ld of a 128x256 f32 accumulator (double
-//               buffered in TMEM, 2 x 256 columns) and the fused epilogue.
+//   warps 2..9  epilogue: tcgen05.ld of a 128x256 f32 accumulator (double
+//               buffered in TMEM, 2 x 256 columns) and the fused epilogue;
+//               two warps per TMEM lane quadrant, each taking 128 columns.
 // The tile shape and the K order are fixed for every M, so a row's result
 // does not depend on which other tasks share the wave (batch invariance).
 //
@@ -27,9 +28,18 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN);
 
+// tanh.approx.f32: the SFU's tanh (max relative error ~2^-11, far below the
+// bf16 rounding of the GELU output).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * x * (1.0f + tanhf(k0 * (x + 0.044715f * x * x * x)));
+  const float x2 = x * x;
+  return 0.5f * x * (1.0f + tanh_approx(k0 * x * fmaf(0.044715f, x2, 1.0f)));
 }
 
 // Fused epilogue of 32 consecutive columns [n0, n0+32) of one row.
@@ -96,11 +106,12 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
       // Rotate pairs (e, e+1) by angle (c*T + li) * f_{e/2}; the angle is
       // assembled from two tables built in f64 on the host.
       const float2* rb = p.rope_base + static_cast<int64_t>(t.rope_slot) * half + (e0 >> 1);
-      const float2* rl = p.rope_local + static_cast<int64_t>(li) * half + (e0 >> 1);
+      // in-chunk table is [dh/2][T]: the warp's 32 rows read 32 consecutive entries
+      const float2* rl = p.rope_local + static_cast<int64_t>(e0 >> 1) * p.T + li;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 cb = __ldg(rb + i);
-        const float2 cl = __ldg(rl + i);
+        const float2 cl = __ldg(rl + static_cast<int64_t>(i) * p.T);
         const float cs = cb.x * cl.x - cb.y * cl.y;
         const float sn = cb.y * cl.x + cb.x * cl.y;
         const float a = v[2 * i], b = v[2 * i + 1];
@@ -144,7 +155,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 8);
     }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -246,6 +257,7 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ---------------- epilogue warps (TMEM lane quadrant = warp % 4)
     const int q = warp & 3;
+    const int chalf = (warp - 2) >> 2;  // which 128 accumulator columns
     int tc = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
       const int mb = tile % n_m, nb = tile / n_m;
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(192, 1)
       const int row = mb * BM + q * 32 + lane;
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ++ch) {
         float v[32];
         tmem_ld32(tbase + ch * 32, v);
         tmem_wait_ld();
@@ -289,7 +301,7 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const Gem
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_tc_kernel<EPI><<<grid, 192, smem, st>>>(*tmA, *tmB, p);
+  gemm_tc_kernel<EPI><<<grid, 320, smem, st>>>(*tmA, *tmB, p);
   return cudaGetLastError();
 }
 

@@ -675,12 +675,13 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
   }
   // RoPE table of in-chunk offsets: (cos, sin) of i * theta^(-2j/dh), f64.
   {
+    // stored [dh/2][T] so that the QKV epilogue's per-row reads coalesce
     std::vector<float2> tab(static_cast<size_t>(m.T) * (m.dh / 2));
     for (int i = 0; i < m.T; ++i)
       for (int j = 0; j < m.dh / 2; ++j) {
         const double ang = static_cast<double>(i) * std::pow(static_cast<double>(m.rope_theta), -2.0 * j / m.dh);
-        tab[static_cast<size_t>(i) * (m.dh / 2) + j] = make_float2(static_cast<float>(std::cos(ang)),
-                                                                   static_cast<float>(std::sin(ang)));
+        tab[static_cast<size_t>(j) * m.T + i] = make_float2(static_cast<float>(std::cos(ang)),
+                                                            static_cast<float>(std::sin(ang)));
       }
     if ((e = cudaMemcpy(ctx->at<float2>(L.rope_local), tab.data(), tab.size() * 8, cudaMemcpyHostToDevice)) !=
         cudaSuccess) {

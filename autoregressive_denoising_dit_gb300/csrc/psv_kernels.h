@@ -31,7 +31,7 @@ struct GemmParams {
   __nv_bfloat16* k_ring;   // [rings][Lr][d]
   __nv_bfloat16* vt_ring;  // [rings][H][dh][Lp]
   int Lr, Lp;
-  const float2* rope_local;  // [T][dh/2]   (cos, sin) of i * f_j
+  const float2* rope_local;  // [dh/2][T]   (cos, sin) of i * f_j
   const float2* rope_base;   // [slots][dh/2] (cos, sin) of c*T * f_j
   // EPI_RESID
   float* h;                // [rows][d]

@@ -2,12 +2,18 @@
 //
 // A [M, K] bf16 activations and W [N, K] bf16 weights (nn.Linear layout)
 // are both K-major, so TMA loads 128-byte-swizzled tiles that feed
-// tcgen05.mma directly.  One CTA per SM, warp-specialised:
-//   warp 0      TMA producer (4-stage smem ring, 48 KB per stage)
-//   warp 1      TMEM allocator + single-thread MMA issuer (128x256x16 MMAs)
-//   warps 2..9  epilogue: tcgen05.ld of a 128x256 f32 accumulator (double
-//               buffered in TMEM, 2 x 256 columns) and the fused epilogue;
-//               two warps per TMEM lane quadrant, each taking 128 columns.
+// tcgen05.mma directly.  CTAs run in pairs (a cluster of two SMs) on 256x256
+// output tiles with 2-SM MMAs (cta_group::2, M = 256): each CTA stages its own
+// 128 rows of A and one 128-row half of the W tile (32 KB per 64-wide k-block,
+// 6 stages), and the even CTA issues every MMA for both.  Per SM this halves
+// the weight traffic and leaves room for a deep TMA pipeline.  Warp roles:
+//   warp 0      TMA producer (both CTAs; completion signalled on the even
+//               CTA's stage barrier)
+//   warp 1      TMEM allocator (both CTAs) + MMA issuer (even CTA only):
+//               256x256x16 MMAs into a double-buffered 2 x 256-column TMEM
+//               accumulator
+//   warps 2..9  epilogue: tcgen05.ld of this CTA's 128 rows, two warps per
+//               TMEM lane quadrant (128 columns each), the fused epilogue.
 // The tile shape and the K order are fixed for every M, so a row's result
 // does not depend on which other tasks share the wave (batch invariance).
 //
@@ -23,10 +29,10 @@ namespace psv {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK, STAGES = kGemmStages;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
-constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN);
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of the W tile
+constexpr uint32_t TMEM_COLS = 512;         // two 256-column accumulators
+constexpr uint32_t IDESC = umma_idesc_bf16(2 * BM, BN);  // 256 x 256 per 2-SM MMA
 
 // tanh.approx.f32: the SFU's tanh (max relative error ~2^-11, far below the
 // bf16 rounding of the GELU output).
@@ -163,44 +169,54 @@ __global__ void __launch_bounds__(320, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);  // used in the even CTA
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* tempty = tfull + 2;                                         // used in the even CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
   const int warp = warp_id(), lane = lane_id();
   const int n_m = (p.M + BM - 1) / BM;
   const int n_n = (p.N + BN - 1) / BN;
-  const int n_tiles = n_m * n_n;
   const int nk = (p.K + BK - 1) / BK;
+  // Tile pairs (m-blocks 2i, 2i+1; same n-block), one per CTA pair at a time,
+  // n-blocks fastest: the pairs running together share their activation
+  // tiles (read from HBM once), and every weight tile stays L2-resident.
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_mp = (n_m + 1) >> 1;
+  const int n_pt = n_mp * n_n;
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], 1);   // the even CTA's producer arrives (with all 64 KB of tx)
+      mbar_init(&empty[i], 1);  // the 2-SM MMA commit arrives in both CTAs
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 8);
+      mbar_init(&tempty[i], 16);  // 8 epilogue warps of each CTA
     }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The peer's barriers must be initialised before anything signals them.
+  cluster_sync();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs)
+      const uint32_t full0 = mapa_shared(&full[0], 0);  // the even CTA's stage barriers
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int mb = tile % n_m, nb = tile / n_m;
+      for (int tp = cid; tp < n_pt && ok; tp += n_clusters) {
+        const int mb = 2 * (tp / n_n) + rank, nb = tp % n_n;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int st = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -208,27 +224,29 @@ __global__ void __launch_bounds__(320, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[st], A_BYTES + B_BYTES);
-          tma_load_2d(sA + st * A_BYTES, &tmA, &full[st], kb * BK, mb * BM);
-          tma_load_3d(sB + st * B_BYTES, &tmB, &full[st], kb * BK, nb * BN, p.wz);
+          if (leader) mbar_arrive_expect_tx(&full[st], 2 * (A_BYTES + B_BYTES));
+          const uint32_t bar = full0 + st * 8;
+          tma_load_2d_pair(sA + st * A_BYTES, &tmA, bar, kb * BK, mb * BM);
+          tma_load_3d_pair(sB + st * B_BYTES, &tmB, bar, kb * BK, nb * BN + rank * (BN / 2), p.wz);
         }
       }
-      if (!ok || error_raised(p.err)) {
-        // Error path: let the loads already issued land before the CTA exits.
-        const uint64_t t0 = global_timer_ns();
-        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
-          while (!mbar_try_wait(&full[j % STAGES], (j / STAGES) & 1)) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) break;
-          }
+      // Wait until the MMAs released the last stages: nothing may still read
+      // this CTA's shared memory or signal it after it leaves (bounded).
+      const uint64_t t0 = global_timer_ns();
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+        while (!mbar_try_wait(&empty[j % STAGES], (j / STAGES) & 1)) {
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even CTA), 2-SM MMAs for the pair
       int it = 0, tc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+      const uint64_t a_desc0 = umma_desc_kmajor(smem_u32(sA), 128);
+      const uint64_t b_desc0 = umma_desc_kmajor(smem_u32(sB), 128);
+      for (int tp = cid; tp < n_pt && ok; tp += n_clusters, ++tc) {
         const int acc = tc & 1;
         const uint32_t aph = (tc >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, p.err, ERR_GEMM_TIMEOUT)) break;
@@ -242,25 +260,23 @@ __global__ void __launch_bounds__(320, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + st * A_BYTES);
-          const uint32_t b0 = smem_u32(sB + st * B_BYTES);
+          const uint64_t a = a_desc0 + static_cast<uint64_t>((st * A_BYTES) >> 4);
+          const uint64_t b = b_desc0 + static_cast<uint64_t>((st * B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            umma_bf16(dtm, umma_desc_kmajor(a0 + k * 32, 128), umma_desc_kmajor(b0 + k * 32, 128),
-                      IDESC, (kb | k) != 0);
-          }
-          umma_commit(&empty[st]);
+          for (int k = 0; k < BK / 16; ++k) umma_bf16_pair(dtm, a + 2 * k, b + 2 * k, IDESC, (kb | k) != 0);
+          umma_commit_pair_mc(&empty[st], 0x3);  // free stage st in both CTAs
         }
-        if (ok) umma_commit(&tfull[acc]);
+        if (ok) umma_commit_pair_mc(&tfull[acc], 0x3);
       }
     }
   } else {
     // ---------------- epilogue warps (TMEM lane quadrant = warp % 4)
     const int q = warp & 3;
     const int chalf = (warp - 2) >> 2;  // which 128 accumulator columns
+    const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
     int tc = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
-      const int mb = tile % n_m, nb = tile / n_m;
+    for (int tp = cid; tp < n_pt; tp += n_clusters, ++tc) {
+      const int mb = 2 * (tp / n_n) + rank, nb = tp % n_n;
       const int acc = tc & 1;
       const uint32_t aph = (tc >> 1) & 1;
       if (!warp_wait(&tfull[acc], aph, p.err, ERR_GEMM_TIMEOUT)) break;
@@ -276,33 +292,55 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);  // the even CTA's barrier
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // Both CTAs must be done before the pair's TMEM is released and either leaves.
+  cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
 template <int EPI>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p,
-                       int grid, cudaStream_t st) {
-  static bool attr_set = false;
+                       int max_ctas, cudaStream_t st) {
+  static int max_clusters = 0;
   const size_t smem = gemm_smem_bytes();
-  if (!attr_set) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    cfg.gridDim = dim3(2);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
   }
-  gemm_tc_kernel<EPI><<<grid, 320, smem, st>>>(*tmA, *tmB, p);
-  return cudaGetLastError();
+  const int n_m = (p.M + BM - 1) / BM, n_n = (p.N + BN - 1) / BN;
+  const int n_pt = ((n_m + 1) / 2) * n_n;
+  int clusters = max_clusters < n_pt ? max_clusters : n_pt;
+  if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *tmA, *tmB, p);
 }
 
 }  // namespace

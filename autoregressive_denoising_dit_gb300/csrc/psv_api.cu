@@ -705,9 +705,10 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint32_t box[2] = {64, 128};
       ok &= encode_bf16(&ctx->tmA_u, 2, ctx->arena + L.u, dims, str, box, SW128);
     }
+    // weight tiles are loaded as two 128-row halves (one per CTA of a cluster)
     auto wmap = [&](CUtensorMap* mp, size_t off, uint64_t K, uint64_t Np, uint64_t Z) {
       uint64_t dims[3] = {K, Np, Z}, str[2] = {K * 2, K * Np * 2};
-      uint32_t box[3] = {64, 256, 1};
+      uint32_t box[3] = {64, 128, 1};
       return encode_bf16(mp, 3, ctx->arena + off, dims, str, box, SW128);
     };
     ok &= wmap(&ctx->tmB_qkv, L.w_qkv, d, L.Npad_qkv, m.B);

@@ -67,7 +67,7 @@ constexpr int kAttnSplitMinTiles = 16;
 int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H);
 size_t attn_part_floats(int max_tasks, int T, int H, int dh);
 
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 4;
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 6;
 size_t gemm_smem_bytes();
 size_t attn_smem_bytes(int dh);
 

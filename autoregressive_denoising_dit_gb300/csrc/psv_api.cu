@@ -147,9 +147,9 @@ Layout plan_layout(const psv_model_desc& m) {
   L.tasks = take(static_cast<size_t>(L.max_tasks) * sizeof(TaskDev));
   L.err = take(256);
   L.scratch = take(static_cast<size_t>(8) * (m.t_embed + 3 * d) * 4 + d * 4);
-  L.attn_pairs = (m.T + 255) / 256;
+  L.attn_pairs = psv::attn_units(m.T);
   L.attn_part = take(psv::attn_part_floats(L.max_tasks, m.T, m.H, m.dh) * 4);
-  L.attn_cnt = take(static_cast<size_t>(L.max_tasks) * m.H * L.attn_pairs * 4);
+  L.attn_cnt = take(psv::attn_counter_ints(L.max_tasks, m.T, m.H) * 4);
   L.total = off;
   return L;
 }
@@ -733,7 +733,7 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint64_t dims[3] = {static_cast<uint64_t>(L.Lp), static_cast<uint64_t>(m.dh),
                           static_cast<uint64_t>(L.n_rings) * m.H};
       uint64_t str[2] = {static_cast<uint64_t>(L.Lp) * 2, static_cast<uint64_t>(L.Lp) * 2 * m.dh};
-      uint32_t box[3] = {64, static_cast<uint32_t>(m.dh), 1};
+      uint32_t box[3] = {64, psv::attn_v_box_rows(m.dh), 1};
       ok &= encode_bf16(&ctx->tmV, 3, ctx->arena + L.vt_ring, dims, str, box, SW128);
     }
     if (!ok) {

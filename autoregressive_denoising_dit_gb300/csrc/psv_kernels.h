@@ -51,21 +51,28 @@ struct AttnParams {
   const TaskDev* tasks;
   __nv_bfloat16* o;        // [rows][d]
   float scale_log2;        // log2(e) / sqrt(dh)
-  // Split-KV partials: per (task, head, query pair) 2 halves x 2 query tiles
-  // of [dh + 2][128] f32 (O transposed, then m, l), and one arrival counter.
+  // Split-KV partials: per (task, head, 256-row query unit) 2 key halves x
+  // 2 CTAs of [dh + 2][128] f32 (O transposed, then m, l), and one arrival
+  // counter per (unit, CTA).
   float* part;
   int* counters;
-  int max_pairs;           // query pairs per (task, head) the partial area is sized for
+  int max_pairs;           // query units per (task, head) the partial area is sized for
   int* err;
 };
 
-// Key tiles (of 128) from which a (task, head, query pair) is split in two
-// halves processed by two CTAs; depends on the task's kv_len only, so the
-// result of a task does not depend on the rest of the wave.
-constexpr int kAttnSplitMinTiles = 16;
-// CTAs an attention launch over these kv lengths needs.
+// Key tiles (of 256) from which a (task, head, query unit) is split in two
+// halves processed by two CTA pairs; depends on the task's kv_len only, so
+// the result of a task does not depend on the rest of the wave.
+constexpr int kAttnSplitMinTiles = 8;
+// Query units of 256 rows (one CTA pair each) per (task, head).
+int attn_units(int T);
+// CTAs (two per pair) an attention launch over these kv lengths needs.
 int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H);
 size_t attn_part_floats(int max_tasks, int T, int H, int dh);
+size_t attn_counter_ints(int max_tasks, int T, int H);
+// Each CTA of a pair loads dh/2 rows of a V^T tile: the box height of the
+// V^T tensor map.
+inline uint32_t attn_v_box_rows(int dh) { return static_cast<uint32_t>(dh / 2); }
 
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 6;
 size_t gemm_smem_bytes();

@@ -28,11 +28,10 @@ struct AttnScratch {
 
 AttnScratch attn_scratch_layout(const psv_attn_problem& p) {
   AttnScratch s{};
-  const int n_pairs = (p.T + 255) / 256;
   s.err = 0;
   s.tasks = 256;
   s.counters = s.tasks + up256(sizeof(TaskDev) * static_cast<size_t>(p.n));
-  s.part = s.counters + up256(sizeof(int) * static_cast<size_t>(p.n) * p.H * n_pairs);
+  s.part = s.counters + up256(sizeof(int) * psv::attn_counter_ints(p.n, p.T, p.H));
   s.total = s.part + up256(psv::attn_part_floats(p.n, p.T, p.H, p.dh) * sizeof(float));
   return s;
 }
@@ -80,16 +79,15 @@ int psv_attention_enqueue(const psv_attn_problem* p, const void* q, const void* 
                         static_cast<uint64_t>(p->n) * p->H};
     uint64_t str[2] = {static_cast<uint64_t>(p->vt_cols) * 2,
                        static_cast<uint64_t>(p->vt_cols) * 2 * p->dh};
-    uint32_t box[3] = {64, static_cast<uint32_t>(p->dh), 1};
+    uint32_t box[3] = {64, psv::attn_v_box_rows(p->dh), 1};
     ok &= psv::encode_bf16_map(&tmV, 3, const_cast<void*>(vt), dims, str, box,
                                CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return PSV_EINVAL;
-  const int n_pairs = (p->T + 255) / 256;
   cudaError_t e;
   // The error word and the counters must start at zero.
   if ((e = cudaMemsetAsync(scratch + L.err, 0, sizeof(int), st)) != cudaSuccess) return PSV_ECUDA;
-  if ((e = cudaMemsetAsync(scratch + L.counters, 0, sizeof(int) * static_cast<size_t>(p->n) * p->H * n_pairs,
+  if ((e = cudaMemsetAsync(scratch + L.counters, 0, sizeof(int) * psv::attn_counter_ints(p->n, p->T, p->H),
                            st)) != cudaSuccess)
     return PSV_ECUDA;
   TaskDev* tasks = reinterpret_cast<TaskDev*>(scratch + L.tasks);
@@ -109,7 +107,7 @@ int psv_attention_enqueue(const psv_attn_problem* p, const void* q, const void* 
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(p->dh)));
   a.part = reinterpret_cast<float*>(scratch + L.part);
   a.counters = reinterpret_cast<int*>(scratch + L.counters);
-  a.max_pairs = n_pairs;
+  a.max_pairs = psv::attn_units(p->T);
   a.err = reinterpret_cast<int*>(scratch + L.err);
   std::vector<int> kv(p->n, p->L);
   const int grid = psv::attn_grid_size(kv.data(), p->n, p->T, p->H);

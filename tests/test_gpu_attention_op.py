@@ -2,8 +2,8 @@
 ABI) against the oracle's explicit-softmax attention on the same bf16 inputs.
 
 Cases span: dh 32 / 64 / 128, ragged query tiles (T not a multiple of 128
-or 256), ragged key tiles, windows long enough to take the two-CTA key split
-(>= 16 key tiles) and the single-key degenerate case.  Tolerance: rel-L2 <=
+or 256), ragged key tiles, windows long enough to take the two-pair key split
+(>= 8 key tiles of 256) and the single-key degenerate case.  Tolerance: rel-L2 <=
 1e-2 per query block (bf16 P and bf16 output against f64).
 """
 import numpy as np

@@ -17,33 +17,50 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // One warp per row; the row stays in registers (MAXV float4 per lane, d up
 // to 128 * MAXV) between the two passes (mean, then centred second moment),
-// so h is read once and no block-wide synchronisation is needed.
+// so h is read once.  The shift/scale vectors of the task of the CTA's first
+// row are staged in shared memory by the whole CTA while the rows load, so
+// no L2 round trip sits between the statistics and the output; a row of
+// another task (only where a task boundary falls inside the CTA's rows)
+// reads its vectors from global memory.
 template <int MAXV>
 __global__ void __launch_bounds__(LN_WARPS * 32)
     ln_mod_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int M, int d, int T,
                   const TaskDev* __restrict__ tasks, const float* __restrict__ table,
                   int use_fmod, int block, int shift_off, int scale_off, float eps) {
-  const int row = blockIdx.x * LN_WARPS + warp_id();
-  if (row >= M) return;
+  extern __shared__ float4 ln_smem[];  // [2][d / 4]: shift, scale
+  const int row0 = blockIdx.x * LN_WARPS;
+  const int row = row0 + warp_id();
   const int lane = lane_id();
-  const TaskDev& t = tasks[row / T];
-  const float* base = table + (use_fmod ? static_cast<int64_t>(t.fmod0)
-                                        : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
-  const float4* shift = reinterpret_cast<const float4*>(base + shift_off);
-  const float4* scale = reinterpret_cast<const float4*>(base + scale_off);
-  const float4* hr = reinterpret_cast<const float4*>(h + static_cast<int64_t>(row) * d);
   const int nv = d >> 2;
-
+  auto mod_base = [&](int r) {
+    const TaskDev& t = tasks[r / T];
+    return table + (use_fmod ? static_cast<int64_t>(t.fmod0)
+                             : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
+  };
   float4 v[MAXV];
   float s = 0.0f;
+  if (row < M) {
+    const float4* hr = reinterpret_cast<const float4*>(h + static_cast<int64_t>(row) * d);
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int k = lane + i * 32;
-    if (k < nv) {
-      v[i] = __ldg(hr + k);
-      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    for (int i = 0; i < MAXV; ++i) {
+      const int k = lane + i * 32;
+      if (k < nv) {
+        v[i] = __ldcs(hr + k);  // read once: keep it out of the way in L2
+        s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
     }
   }
+  {
+    const float* base = mod_base(row0);
+    const float4* shift = reinterpret_cast<const float4*>(base + shift_off);
+    const float4* scale = reinterpret_cast<const float4*>(base + scale_off);
+    for (int k = threadIdx.x; k < nv; k += LN_WARPS * 32) {
+      ln_smem[k] = __ldg(shift + k);
+      ln_smem[nv + k] = __ldg(scale + k);
+    }
+  }
+  __syncthreads();
+  if (row >= M) return;
   const float mean = warp_sum(s) / static_cast<float>(d);
   float q = 0.0f;
 #pragma unroll
@@ -55,12 +72,20 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
     }
   }
   const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(d) + eps);
+  const bool own_task = (row / T) == (row0 / T);
+  const float4* shift = ln_smem;
+  const float4* scale = ln_smem + nv;
+  if (!own_task) {
+    const float* base = mod_base(row);
+    shift = reinterpret_cast<const float4*>(base + shift_off);
+    scale = reinterpret_cast<const float4*>(base + scale_off);
+  }
   uint2* yr = reinterpret_cast<uint2*>(y + static_cast<int64_t>(row) * d);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int k = lane + i * 32;
     if (k < nv) {
-      const float4 sh = __ldg(shift + k), sc = __ldg(scale + k);
+      const float4 sh = shift[k], sc = scale[k];
       uint2 o;
       o.x = pack_bf16x2((v[i].x - mean) * rstd * (1.0f + sc.x) + sh.x,
                         (v[i].y - mean) * rstd * (1.0f + sc.y) + sh.y);
@@ -188,9 +213,11 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
   if (d % 4 != 0) return cudaErrorInvalidValue;
   const int nv = d / 4;
   const int grid = (M + LN_WARPS - 1) / LN_WARPS;
+  const size_t smem = 2 * static_cast<size_t>(nv) * sizeof(float4);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
 #define PSV_LN_LAUNCH(V)                                                                     \
-  ln_mod_kernel<V><<<grid, LN_WARPS * 32, 0, st>>>(h, y, M, d, T, tasks, table, use_fmod, \
-                                                   block, shift_off, scale_off, eps)
+  ln_mod_kernel<V><<<grid, LN_WARPS * 32, smem, st>>>(h, y, M, d, T, tasks, table,         \
+                                                      use_fmod, block, shift_off, scale_off, eps)
   if (nv <= 32 * 1) PSV_LN_LAUNCH(1);
   else if (nv <= 32 * 2) PSV_LN_LAUNCH(2);
   else if (nv <= 32 * 4) PSV_LN_LAUNCH(4);

@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);  // the even CTA's barrier
+      // CTA-scope release: the arrival only orders this warp's TMEM reads
+      // (tcgen05 fence above) before the MMAs that overwrite the accumulator.
+      if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);  // the even CTA's barrier
     }
   }
 

@@ -4,8 +4,8 @@
 // are both K-major, so TMA loads 128-byte-swizzled tiles that feed
 // tcgen05.mma directly.  CTAs run in pairs (a cluster of two SMs) on 256x256
 // output tiles with 2-SM MMAs (cta_group::2, M = 256): each CTA stages its own
-// 128 rows of A and one 128-row half of the W tile (32 KB per 64-wide k-block,
-// 6 stages), and the even CTA issues every MMA for both.  Per SM this halves
+// 128 rows of A and one 128-row half of the W tile (64 KB per 128-wide k-block,
+// 3 stages), and the even CTA issues every MMA for both.  Per SM this halves
 // the weight traffic and leaves room for a deep TMA pipeline.  Warp roles:
 //   warp 0      TMA producer (both CTAs; completion signalled on the even
 //               CTA's stage barrier)
@@ -29,8 +29,12 @@ namespace psv {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK, STAGES = kGemmStages;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
-constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of the W tile
+constexpr int KA = BK / 64;                 // 128-byte swizzle atoms along K per stage
+constexpr int A_ATOM = BM * 128;            // 16 KB: 128 rows x 64 k
+constexpr int B_ATOM = (BN / 2) * 128;      // 16 KB: 128 W rows x 64 k
+constexpr int A_BYTES = KA * A_ATOM;        // this CTA's 128 rows of A
+constexpr int B_BYTES = KA * B_ATOM;        // this CTA's half of the W tile
+static_assert(BK % 64 == 0, "k-block is a whole number of swizzle atoms");
 constexpr uint32_t TMEM_COLS = 512;         // two 256-column accumulators
 constexpr uint32_t IDESC = umma_idesc_bf16(2 * BM, BN);  // 256 x 256 per 2-SM MMA
 
@@ -226,8 +230,12 @@ __global__ void __launch_bounds__(320, 1)
           }
           if (leader) mbar_arrive_expect_tx(&full[st], 2 * (A_BYTES + B_BYTES));
           const uint32_t bar = full0 + st * 8;
-          tma_load_2d_pair(sA + st * A_BYTES, &tmA, bar, kb * BK, mb * BM);
-          tma_load_3d_pair(sB + st * B_BYTES, &tmB, bar, kb * BK, nb * BN + rank * (BN / 2), p.wz);
+#pragma unroll
+          for (int a = 0; a < KA; ++a) {
+            tma_load_2d_pair(sA + st * A_BYTES + a * A_ATOM, &tmA, bar, kb * BK + a * 64, mb * BM);
+            tma_load_3d_pair(sB + st * B_BYTES + a * B_ATOM, &tmB, bar, kb * BK + a * 64,
+                             nb * BN + rank * (BN / 2), p.wz);
+          }
         }
       }
       // Wait until the MMAs released the last stages: nothing may still read
@@ -263,7 +271,12 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t a = a_desc0 + static_cast<uint64_t>((st * A_BYTES) >> 4);
           const uint64_t b = b_desc0 + static_cast<uint64_t>((st * B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) umma_bf16_pair(dtm, a + 2 * k, b + 2 * k, IDESC, (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k) {
+            // k-step k: atom k / 4, 32 bytes per step inside the atom
+            const uint32_t oa = ((k >> 2) * A_ATOM + (k & 3) * 32) >> 4;
+            const uint32_t ob = ((k >> 2) * B_ATOM + (k & 3) * 32) >> 4;
+            umma_bf16_pair(dtm, a + oa, b + ob, IDESC, (kb | k) != 0);
+          }
           umma_commit_pair_mc(&empty[st], 0x3);  // free stage st in both CTAs
         }
         if (ok) umma_commit_pair_mc(&tfull[acc], 0x3);

@@ -36,6 +36,8 @@ constexpr int A_BYTES = KA * A_ATOM;        // this CTA's 128 rows of A
 constexpr int B_BYTES = KA * B_ATOM;        // this CTA's half of the W tile
 static_assert(BK % 64 == 0, "k-block is a whole number of swizzle atoms");
 constexpr uint32_t TMEM_COLS = 512;         // two 256-column accumulators
+constexpr int EPI_WARPS = 8;
+constexpr int STAGE_BYTES = 32 * 32 * 4;    // per epilogue warp: a 32 x 32 f32 box
 constexpr uint32_t IDESC = umma_idesc_bf16(2 * BM, BN);  // 256 x 256 per 2-SM MMA
 
 // tanh.approx.f32: the SFU's tanh (max relative error ~2^-11, far below the
@@ -92,20 +94,6 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
       w.w = pack_bf16x2(gelu_tanh(v[8 * i + 6]), gelu_tanh(v[8 * i + 7]));
       dst[i] = w;
     }
-  } else if (EPI == EPI_RESID) {
-    const float4* g4 = reinterpret_cast<const float4*>(
-        p.mod + t.mod0 + static_cast<int64_t>(p.block) * 6 * p.d + p.gate_off + n0);
-    float4* h4 = reinterpret_cast<float4*>(p.h + static_cast<int64_t>(row) * p.d + n0);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 g = __ldg(g4 + i);
-      float4 hv = h4[i];
-      hv.x += g.x * v[4 * i];
-      hv.y += g.y * v[4 * i + 1];
-      hv.z += g.z * v[4 * i + 2];
-      hv.w += g.w * v[4 * i + 3];
-      h4[i] = hv;
-    }
   } else if (EPI == EPI_QKV) {
     const int sec = n0 / p.d;  // 0 = q, 1 = k, 2 = v
     const int j0 = n0 - sec * p.d;
@@ -157,6 +145,61 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
   }
 }
 
+// ---- gated residual through a TMA reduce-add: h[rows][cols] += box.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x,
+                                                  int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until the source shared memory of every committed bulk operation was read.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Gated residual of one warp's 32 rows x 32 columns: h += gate * (acc + b).
+// The products are staged as a 128-byte-swizzled [32][32] f32 box and added
+// into h by one TMA reduce (the add happens in L2 on whole lines, instead of
+// 32 partial-line read-modify-writes per warp instruction).  Every element
+// gets exactly one add, so the result is deterministic.  Rows past M add 0.
+__device__ __forceinline__ void resid_chunk(const GemmParams& p, const CUtensorMap* tmC,
+                                            float* stage, int row, int row0, int n0, float* v) {
+  const int lane = lane_id();
+  if (row < p.M && n0 < p.N) {
+    const TaskDev& t = p.tasks[row / p.T];
+    const float4* b4 = reinterpret_cast<const float4*>(p.bias + n0);
+    const float4* g4 = reinterpret_cast<const float4*>(
+        p.mod + t.mod0 + static_cast<int64_t>(p.block) * 6 * p.d + p.gate_off + n0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 bb = __ldg(b4 + i), g = __ldg(g4 + i);
+      v[4 * i] = g.x * (v[4 * i] + bb.x);
+      v[4 * i + 1] = g.y * (v[4 * i + 1] + bb.y);
+      v[4 * i + 2] = g.z * (v[4 * i + 2] + bb.z);
+      v[4 * i + 3] = g.w * (v[4 * i + 3] + bb.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+  }
+  // The previous box of this warp must have been read out of the staging buffer.
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  float4* st4 = reinterpret_cast<float4*>(stage);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st4[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_reduce_add_2d(tmC, stage, n0, row0);
+    bulk_commit();
+  }
+}
+
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   int ok = 0;
@@ -167,13 +210,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
 template <int EPI>
 __global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);  // used in the even CTA
+  uint8_t* sC = sB + STAGES * B_BYTES;  // epilogue staging, STAGE_BYTES per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sC + EPI_WARPS * STAGE_BYTES);  // even CTA
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;                                         // used in the even CTA
@@ -287,6 +332,7 @@ __global__ void __launch_bounds__(320, 1)
     const int q = warp & 3;
     const int chalf = (warp - 2) >> 2;  // which 128 accumulator columns
     const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
+    float* stage = reinterpret_cast<float*>(sC + (warp - 2) * STAGE_BYTES);
     int tc = 0;
     for (int tp = cid; tp < n_pt; tp += n_clusters, ++tc) {
       const int mb = 2 * (tp / n_n) + rank, nb = tp % n_n;
@@ -301,7 +347,11 @@ __global__ void __launch_bounds__(320, 1)
         float v[32];
         tmem_ld32(tbase + ch * 32, v);
         tmem_wait_ld();
-        epilogue32<EPI>(p, row, nb * BN + ch * 32, v);
+        if constexpr (EPI == EPI_RESID) {
+          resid_chunk(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+        } else {
+          epilogue32<EPI>(p, row, nb * BN + ch * 32, v);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -309,6 +359,8 @@ __global__ void __launch_bounds__(320, 1)
       // (tcgen05 fence above) before the MMAs that overwrite the accumulator.
       if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);  // the even CTA's barrier
     }
+    // The staged reductions must have completed before the CTA exits.
+    if (EPI == EPI_RESID && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -323,8 +375,8 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 template <int EPI>
-cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmParams& p,
-                       int max_ctas, cudaStream_t st) {
+cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
+                       const GemmParams& p, int max_ctas, cudaStream_t st) {
   static int max_clusters = 0;
   const size_t smem = gemm_smem_bytes();
   cudaLaunchConfig_t cfg = {};
@@ -355,22 +407,25 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const Gem
   int clusters = max_clusters < n_pt ? max_clusters : n_pt;
   if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
   cfg.gridDim = dim3(2 * clusters);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *tmA, *tmB, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *tmA, *tmB, *tmC, p);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() {
-  return 1024 + STAGES * (A_BYTES + B_BYTES) + (2 * STAGES + 4) * sizeof(uint64_t) + 16;
+  return 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_WARPS * STAGE_BYTES +
+         (2 * STAGES + 4) * sizeof(uint64_t) + 16;
 }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const GemmParams& p, int grid, cudaStream_t st) {
+                        const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st) {
+  if (epi == EPI_RESID && !tmC) return cudaErrorInvalidValue;
+  const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
   switch (epi) {
-    case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, p, grid, st);
-    case EPI_RESID: return launch_one<EPI_RESID>(tmA, tmB, p, grid, st);
-    case EPI_GELU: return launch_one<EPI_GELU>(tmA, tmB, p, grid, st);
-    case EPI_EULER: return launch_one<EPI_EULER>(tmA, tmB, p, grid, st);
+    case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, c, p, grid, st);
+    case EPI_RESID: return launch_one<EPI_RESID>(tmA, tmB, c, p, grid, st);
+    case EPI_GELU: return launch_one<EPI_GELU>(tmA, tmB, c, p, grid, st);
+    case EPI_EULER: return launch_one<EPI_EULER>(tmA, tmB, c, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -169,15 +169,27 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 
 }  // namespace
 
-bool psv::encode_bf16_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
-                          const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+namespace {
+bool encode_map(CUtensorMapDataType dt, CUtensorMap* map, int rank, void* base,
+                const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                CUtensorMapSwizzle sw) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, dt, rank, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool psv::encode_bf16_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  return encode_map(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, map, rank, base, dims, strides, box, sw);
+}
+
+bool psv::encode_f32_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  return encode_map(CU_TENSOR_MAP_DATA_TYPE_FLOAT32, map, rank, base, dims, strides, box, sw);
 }
 
 namespace {
@@ -251,6 +263,7 @@ struct psv_ctx {
   cudaEvent_t wave_ev[kWaveEvents] = {};
   // tensor maps
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
+  CUtensorMap tmC_h;  // f32 h, the target of the gated-residual TMA reductions
   // executor
   bool use_graphs = true;
   std::map<int64_t, int> shape_seen;
@@ -461,7 +474,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.rope_local = ctx->at<float2>(L.rope_local);
       p.rope_base = ctx->at<float2>(L.rope_base);
       run.run(K_GEMM_QKV, 2.0 * Md * 3 * d, Md * 2 + 3.0 * d * d * 2 + 3 * Md * 2, [&] {
-        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // window attention
@@ -499,7 +512,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 2 * d;
       run.run(K_GEMM_O, 2.0 * Md * d, Md * 2 + 1.0 * d * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, &ctx->tmC_h, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // LN2 + modulation
@@ -517,7 +530,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.bias = ctx->at<float>(L.b_up) + static_cast<size_t>(b) * F;
       p.u = ctx->at<__nv_bfloat16>(L.u);
       run.run(K_GEMM_UP, 2.0 * Md * F, Md * 2 + 1.0 * F * d * 2 + static_cast<double>(M) * F * 2, [&] {
-        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // down + gated residual (gate2)
@@ -532,7 +545,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 5 * d;
       run.run(K_GEMM_DOWN, 2.0 * Md * F, static_cast<double>(M) * F * 2 + 1.0 * F * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, &ctx->tmC_h, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     if (tap && b == ctx->tap_block && run.err == cudaSuccess)
@@ -552,7 +565,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     p.bias = ctx->at<float>(L.b_out);
     p.state = ctx->at<float>(L.state);
     run.run(K_GEMM_FINAL, 2.0 * Md * m.C, Md * 2 + static_cast<double>(M) * m.C * 8, [&] {
-      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, p, gemm_grid(ctx, M, p.N), st);
+      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, nullptr, p, gemm_grid(ctx, M, p.N), st);
     });
   }
   return run.err;
@@ -704,6 +717,12 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint64_t dims[2] = {F, Mx}, str[1] = {F * 2};
       uint32_t box[2] = {64, 128};
       ok &= encode_bf16(&ctx->tmA_u, 2, ctx->arena + L.u, dims, str, box, SW128);
+    }
+    {
+      // h as the target of 32 x 32 f32 boxes (128-byte rows, swizzled)
+      uint64_t dims[2] = {d, Mx}, str[1] = {d * 4};
+      uint32_t box[2] = {32, 32};
+      ok &= psv::encode_f32_map(&ctx->tmC_h, 2, ctx->arena + L.h, dims, str, box, SW128);
     }
     // weight tiles are loaded as two 128-row halves (one per CTA of a cluster)
     auto wmap = [&](CUtensorMap* mp, size_t off, uint64_t K, uint64_t Np, uint64_t Z) {

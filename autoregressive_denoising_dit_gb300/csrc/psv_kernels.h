@@ -78,8 +78,10 @@ constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 128, kGemmStages = 3;
 size_t gemm_smem_bytes();
 size_t attn_smem_bytes(int dh);
 
+// tmC: f32 map of h ([rows][d], box 32 x 32, 128-byte swizzle) for EPI_RESID,
+// which adds its output with TMA reductions; the other epilogues ignore it.
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const GemmParams& p, int grid, cudaStream_t st);
+                        const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, const AttnParams& p, int n_tasks, int grid,
                              cudaStream_t st);
@@ -107,5 +109,8 @@ cudaError_t launch_fill_attn_tasks(TaskDev* tasks, int n, int T, int L, cudaStre
 // 1..rank-1); false if the driver entry point or the arguments are rejected.
 bool encode_bf16_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
                      const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
+// The same for f32 elements.
+bool encode_f32_map(CUtensorMap* map, int rank, void* base, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
 
 }  // namespace psv

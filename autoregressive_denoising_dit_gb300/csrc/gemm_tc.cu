@@ -54,7 +54,8 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanh_approx(k0 * x * fmaf(0.044715f, x2, 1.0f)));
 }
 
-// Fused epilogue of 32 consecutive columns [n0, n0+32) of one row.
+// Fused epilogue of 32 consecutive columns [n0, n0+32) of one row (QKV and
+// velocity head; the residual and GELU epilogues write through staged TMA boxes).
 template <int EPI>
 __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0, float* v) {
   if (row >= p.M || n0 >= p.N) return;
@@ -83,18 +84,7 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
     v[4 * i + 3] += bb.w;
   }
 
-  if (EPI == EPI_GELU) {
-    uint4* dst = reinterpret_cast<uint4*>(p.u + static_cast<int64_t>(row) * p.N + n0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 w;
-      w.x = pack_bf16x2(gelu_tanh(v[8 * i + 0]), gelu_tanh(v[8 * i + 1]));
-      w.y = pack_bf16x2(gelu_tanh(v[8 * i + 2]), gelu_tanh(v[8 * i + 3]));
-      w.z = pack_bf16x2(gelu_tanh(v[8 * i + 4]), gelu_tanh(v[8 * i + 5]));
-      w.w = pack_bf16x2(gelu_tanh(v[8 * i + 6]), gelu_tanh(v[8 * i + 7]));
-      dst[i] = w;
-    }
-  } else if (EPI == EPI_QKV) {
+  if (EPI == EPI_QKV) {
     const int sec = n0 / p.d;  // 0 = q, 1 = k, 2 = v
     const int j0 = n0 - sec * p.d;
     const int head = j0 / p.dh;
@@ -196,6 +186,45 @@ __device__ __forceinline__ void resid_chunk(const GemmParams& p, const CUtensorM
   __syncwarp();
   if (lane == 0) {
     tma_reduce_add_2d(tmC, stage, n0, row0);
+    bulk_commit();
+  }
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// GELU of one warp's 32 rows x 64 columns, staged as a 128-byte-swizzled
+// [32][64] bf16 box and written by one TMA store (whole 128-byte lines).
+// Rows past M are written as zeros.
+__device__ __forceinline__ void gelu_chunk64(const GemmParams& p, const CUtensorMap* tmC,
+                                             void* stage, int row, int row0, int n0, float* v) {
+  const int lane = lane_id();
+  uint32_t w[32];
+  if (row < p.M) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int n = n0 + 2 * i;
+      const float b0 = n < p.N ? __ldg(p.bias + n) : 0.0f;
+      const float b1 = n + 1 < p.N ? __ldg(p.bias + n + 1) : 0.0f;
+      w[i] = pack_bf16x2(gelu_tanh(v[2 * i] + b0), gelu_tanh(v[2 * i + 1] + b1));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = 0u;
+  }
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  uint4* st4 = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st4[lane * 8 + (j ^ (lane & 7))] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, stage, n0, row0);
     bulk_commit();
   }
 }
@@ -342,15 +371,26 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
       const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      if constexpr (EPI == EPI_GELU) {
 #pragma unroll 1
-      for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ++ch) {
-        float v[32];
-        tmem_ld32(tbase + ch * 32, v);
-        tmem_wait_ld();
-        if constexpr (EPI == EPI_RESID) {
-          resid_chunk(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
-        } else {
-          epilogue32<EPI>(p, row, nb * BN + ch * 32, v);
+        for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ch += 2) {
+          float v[64];
+          tmem_ld32(tbase + ch * 32, v);
+          tmem_ld32(tbase + ch * 32 + 32, v + 32);
+          tmem_wait_ld();
+          gelu_chunk64(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ++ch) {
+          float v[32];
+          tmem_ld32(tbase + ch * 32, v);
+          tmem_wait_ld();
+          if constexpr (EPI == EPI_RESID) {
+            resid_chunk(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+          } else {
+            epilogue32<EPI>(p, row, nb * BN + ch * 32, v);
+          }
         }
       }
       tc_fence_before();
@@ -359,8 +399,8 @@ __global__ void __launch_bounds__(320, 1)
       // (tcgen05 fence above) before the MMAs that overwrite the accumulator.
       if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);  // the even CTA's barrier
     }
-    // The staged reductions must have completed before the CTA exits.
-    if (EPI == EPI_RESID && lane == 0) bulk_wait_all();
+    // The staged stores and reductions must have completed before the CTA exits.
+    if ((EPI == EPI_RESID || EPI == EPI_GELU) && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -419,7 +459,7 @@ size_t gemm_smem_bytes() {
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st) {
-  if (epi == EPI_RESID && !tmC) return cudaErrorInvalidValue;
+  if ((epi == EPI_RESID || epi == EPI_GELU) && !tmC) return cudaErrorInvalidValue;
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
   switch (epi) {
     case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, c, p, grid, st);

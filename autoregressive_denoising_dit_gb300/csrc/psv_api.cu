@@ -264,6 +264,7 @@ struct psv_ctx {
   // tensor maps
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
   CUtensorMap tmC_h;  // f32 h, the target of the gated-residual TMA reductions
+  CUtensorMap tmC_u;  // bf16 u, written by the GELU epilogue's TMA stores
   // executor
   bool use_graphs = true;
   std::map<int64_t, int> shape_seen;
@@ -530,7 +531,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.bias = ctx->at<float>(L.b_up) + static_cast<size_t>(b) * F;
       p.u = ctx->at<__nv_bfloat16>(L.u);
       run.run(K_GEMM_UP, 2.0 * Md * F, Md * 2 + 1.0 * F * d * 2 + static_cast<double>(M) * F * 2, [&] {
-        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, nullptr, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, &ctx->tmC_u, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // down + gated residual (gate2)
@@ -717,6 +718,8 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint64_t dims[2] = {F, Mx}, str[1] = {F * 2};
       uint32_t box[2] = {64, 128};
       ok &= encode_bf16(&ctx->tmA_u, 2, ctx->arena + L.u, dims, str, box, SW128);
+      uint32_t obox[2] = {64, 32};
+      ok &= encode_bf16(&ctx->tmC_u, 2, ctx->arena + L.u, dims, str, obox, SW128);
     }
     {
       // h as the target of 32 x 32 f32 boxes (128-byte rows, swizzled)

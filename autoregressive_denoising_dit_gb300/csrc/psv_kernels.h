@@ -78,8 +78,9 @@ constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 128, kGemmStages = 3;
 size_t gemm_smem_bytes();
 size_t attn_smem_bytes(int dh);
 
-// tmC: f32 map of h ([rows][d], box 32 x 32, 128-byte swizzle) for EPI_RESID,
-// which adds its output with TMA reductions; the other epilogues ignore it.
+// tmC: output map of the epilogues that write through TMA: f32 h ([rows][d],
+// box 32 x 32, 128-byte swizzle) for EPI_RESID (TMA reduce-add), bf16 u
+// ([rows][F], box 64 x 32, 128-byte swizzle) for EPI_GELU; the others ignore it.
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,

@@ -54,8 +54,13 @@ class Session:
     def open_stream(self, cond):
         return _psv.psv_open_stream(self.ctx, cond)
 
-    def submit(self, sid, noise):
-        _psv.psv_submit_chunk(self.ctx, sid, noise)
+    def submit(self, sid, noise, cond=None):
+        """Submit the stream's next chunk; ``cond`` [d] gives the chunk its own
+        conditioning vector (needs ``flags`` with PSV_FLAG_CHUNK_COND)."""
+        if cond is None:
+            _psv.psv_submit_chunk(self.ctx, sid, noise)
+        else:
+            _psv.psv_submit_chunk_cond(self.ctx, sid, noise, cond)
 
     def run_wave(self) -> int:
         return _psv.psv_run_wave(self.ctx)

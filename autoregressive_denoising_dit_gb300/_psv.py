@@ -24,6 +24,7 @@ PSV_EDEVICE = -6
 
 PSV_FLAG_PLAN_ONLY = 1
 PSV_FLAG_SEQUENTIAL = 2
+PSV_FLAG_CHUNK_COND = 4
 
 PSV_DTYPE_F32 = 0
 PSV_DTYPE_BF16 = 1
@@ -41,7 +42,7 @@ WEIGHT_IDS = {
 # Every exported entry point of psv.h.
 EXPORTS = [
     "psv_arena_bytes", "psv_create", "psv_load_weights", "psv_open_stream",
-    "psv_submit_chunk", "psv_run_wave", "psv_poll_chunk", "psv_sync",
+    "psv_submit_chunk", "psv_submit_chunk_cond", "psv_run_wave", "psv_poll_chunk", "psv_sync",
     "psv_wave_plan", "psv_close_stream", "psv_destroy", "psv_last_error",
     "psv_set_graphs", "psv_set_profiling", "psv_kernel_times", "psv_debug_tap",
     "psv_debug_read_kv", "psv_attention_scratch_bytes", "psv_attention",
@@ -64,7 +65,7 @@ class Weight(ctypes.Structure):
 
 class Task(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("stream", "chunk", "step", "slot", "kv_len",
-                                              "row_off", "state_slot")]
+                                              "row_off", "state_slot", "cond_table")]
 
     def as_tuple(self):
         return (self.stream, self.chunk, self.step, self.slot, self.kv_len, self.row_off,
@@ -105,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "psv_load_weights": (i32, [vp, ctypes.POINTER(Weight), i32]),
             "psv_open_stream": (i32, [vp, vp, ctypes.POINTER(i32)]),
             "psv_submit_chunk": (i32, [vp, i32, vp]),
+            "psv_submit_chunk_cond": (i32, [vp, i32, vp, vp]),
             "psv_run_wave": (i32, [vp, ctypes.POINTER(i32)]),
             "psv_poll_chunk": (i32, [vp, i32, vp, ctypes.POINTER(i64)]),
             "psv_sync": (i32, [vp, i32]),
@@ -199,6 +201,12 @@ def psv_submit_chunk(ctx, sid: int, noise: np.ndarray | None) -> None:
     _check(ctx, lib().psv_submit_chunk(ctx, sid, ptr))
 
 
+def psv_submit_chunk_cond(ctx, sid: int, noise: np.ndarray | None, cond: np.ndarray | None) -> None:
+    pn = None if noise is None else _fptr(noise)
+    pc = None if cond is None else _fptr(cond)
+    _check(ctx, lib().psv_submit_chunk_cond(ctx, sid, pn, pc))
+
+
 def psv_run_wave(ctx) -> int:
     n = ctypes.c_int()
     _check(ctx, lib().psv_run_wave(ctx, ctypes.byref(n)))
@@ -220,11 +228,15 @@ def psv_sync(ctx, timeout_ms: int = -1) -> None:
     _check(ctx, lib().psv_sync(ctx, timeout_ms))
 
 
-def psv_wave_plan(ctx) -> list:
+def psv_wave_plan(ctx, cond_tables: bool = False) -> list:
+    """Tasks of the next wave as tuples (stream, chunk, step, slot, kv_len,
+    row_off, state_slot), plus cond_table last when ``cond_tables``."""
     n = ctypes.c_int()
     _check(ctx, lib().psv_wave_plan(ctx, None, 0, ctypes.byref(n)))
     buf = (Task * max(1, n.value))()
     _check(ctx, lib().psv_wave_plan(ctx, buf, n.value, ctypes.byref(n)))
+    if cond_tables:
+        return [buf[i].as_tuple() + (buf[i].cond_table,) for i in range(n.value)]
     return [buf[i].as_tuple() for i in range(n.value)]
 
 

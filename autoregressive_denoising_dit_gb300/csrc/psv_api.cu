@@ -47,6 +47,7 @@ struct Layout {
   // derived sizes
   int Npad_qkv, Npad_o, Npad_up, Npad_down, Npad_out;
   int Lr, Lp, n_rings, n_slots, max_tasks, M_max;
+  int n_ctabs;  // conditioning tables: one per stream, plus one per chunk slot with PSV_FLAG_CHUNK_COND
   // byte offsets into the arena
   size_t w_qkv, w_o, w_up, w_down, w_mod;
   size_t b_qkv, b_o, b_up, b_down, b_mod;
@@ -55,6 +56,8 @@ struct Layout {
   size_t k_ring, vt_ring, rings_end;
   size_t h, y, q, o, u, acts_end;
   size_t state, mod, fmod, rope_local, rope_base, tasks, err, scratch;
+  size_t temb_in;  // timestep sinusoids of t_0..t_{S-1}, f32 [S][t_embed]
+  size_t ccond;    // per-chunk conditioning vectors, f32 [n_slots][d] (PSV_FLAG_CHUNK_COND)
   size_t attn_part, attn_cnt;  // split-KV partials and arrival counters
   int attn_pairs;
   size_t total;
@@ -84,6 +87,11 @@ int validate(const psv_model_desc* d, std::string* why) {
   if (rows > (1 << 30) / 8) return fail("wave too large");
   const int64_t lr = static_cast<int64_t>(d->W + 1) * d->T;
   if (lr > (1 << 28)) return fail("KV window too long");
+  // adaLN table offsets are 32-bit float offsets (TaskDev.mod0)
+  const int64_t inflight = d->max_inflight > 0 ? d->max_inflight : d->S + 4;
+  const int64_t ctabs = d->max_streams + ((d->flags & PSV_FLAG_CHUNK_COND) ? d->max_streams * inflight : 0);
+  if (ctabs * d->S * d->B * 6 * static_cast<int64_t>(d->d) >= (int64_t{1} << 31))
+    return fail("adaLN tables too large (streams x in-flight chunks x steps x blocks x 6d)");
   return PSV_OK;
 }
 
@@ -101,6 +109,7 @@ Layout plan_layout(const psv_model_desc& m) {
   L.Lp = static_cast<int>(round_up(L.Lr, 64));
   L.n_rings = m.max_streams * m.B * m.S;
   L.n_slots = m.max_streams * inflight_of(m);
+  L.n_ctabs = m.max_streams + ((m.flags & PSV_FLAG_CHUNK_COND) ? L.n_slots : 0);
   L.max_tasks = m.max_streams * m.S;
   L.M_max = static_cast<int>(round_up(static_cast<int64_t>(L.max_tasks) * m.T, 128));
   size_t off = 0;
@@ -140,8 +149,10 @@ Layout plan_layout(const psv_model_desc& m) {
   L.u = take(static_cast<size_t>(L.M_max) * F * 2);
   L.acts_end = off;
   L.state = take(static_cast<size_t>(L.n_slots) * m.T * C * 4);
-  L.mod = take(static_cast<size_t>(m.max_streams) * S * B * 6 * d * 4);
-  L.fmod = take(static_cast<size_t>(m.max_streams) * S * 2 * d * 4);
+  L.mod = take(static_cast<size_t>(L.n_ctabs) * S * B * 6 * d * 4);
+  L.fmod = take(static_cast<size_t>(L.n_ctabs) * S * 2 * d * 4);
+  L.temb_in = take(static_cast<size_t>(S) * m.t_embed * 4);
+  L.ccond = take((m.flags & PSV_FLAG_CHUNK_COND) ? static_cast<size_t>(L.n_slots) * d * 4 : 4);
   L.rope_local = take(static_cast<size_t>(m.T) * (m.dh / 2) * 8);
   L.rope_base = take(static_cast<size_t>(L.n_slots) * (m.dh / 2) * 8);
   L.tasks = take(static_cast<size_t>(L.max_tasks) * sizeof(TaskDev));
@@ -224,6 +235,7 @@ struct StreamState {
   int64_t n_sub = 0, n_polled = 0;
   int64_t done[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   std::vector<int64_t> finish_wave;  // per state slot: wave that finished the chunk
+  std::vector<char> own_cond;        // per state slot: chunk submitted with its own cond
 };
 
 struct ProfRec {
@@ -259,6 +271,7 @@ struct psv_ctx {
   float2* h_rope = nullptr;   // [n_slots][dh/2]
   float* h_out = nullptr;     // [T*C]
   float* h_misc = nullptr;    // conditioning staging
+  float* h_ccond = nullptr;   // [n_slots][d] per-chunk conditioning staging
   size_t h_misc_bytes = 0;
   cudaEvent_t wave_ev[kWaveEvents] = {};
   // tensor maps
@@ -337,6 +350,7 @@ void plan_wave(const psv_ctx* ctx, std::vector<psv_task>* out) {
       t.slot = static_cast<int32_t>(c % (m.W + 1));
       t.kv_len = static_cast<int32_t>((std::min<int64_t>(c, m.W) + 1) * m.T);
       t.state_slot = sid * ctx->inflight + static_cast<int32_t>(c % ctx->inflight);
+      t.cond_table = st.own_cond[static_cast<size_t>(c % ctx->inflight)] ? m.max_streams + t.state_slot : sid;
       out->push_back(t);
     }
   }
@@ -363,8 +377,8 @@ TaskDev to_dev(const psv_ctx* ctx, const psv_task& t) {
   d.ring0 = t.stream * m.B * m.S + t.step;
   d.slot = t.slot;
   d.kv_len = t.kv_len;
-  d.mod0 = (t.stream * m.S + t.step) * m.B * 6 * m.d;
-  d.fmod0 = (t.stream * m.S + t.step) * 2 * m.d;
+  d.mod0 = (t.cond_table * m.S + t.step) * m.B * 6 * m.d;
+  d.fmod0 = (t.cond_table * m.S + t.step) * 2 * m.d;
   const double ts = 1.0 - static_cast<double>(t.step) / m.S;
   const double tn = 1.0 - static_cast<double>(t.step + 1) / m.S;
   d.dt = static_cast<float>(tn - ts);
@@ -675,7 +689,9 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       cudaMallocHost(&ctx->h_noise, tc * 4 * L.n_slots) != cudaSuccess ||
       cudaMallocHost(&ctx->h_rope, static_cast<size_t>(L.n_slots) * (m.dh / 2) * 8) != cudaSuccess ||
       cudaMallocHost(&ctx->h_out, tc * 4) != cudaSuccess ||
-      cudaMallocHost(&ctx->h_misc, ctx->h_misc_bytes) != cudaSuccess) {
+      cudaMallocHost(&ctx->h_misc, ctx->h_misc_bytes) != cudaSuccess ||
+      ((m.flags & PSV_FLAG_CHUNK_COND) &&
+       cudaMallocHost(&ctx->h_ccond, static_cast<size_t>(L.n_slots) * m.d * 4) != cudaSuccess)) {
     set_err(ctx, PSV_ENOMEM, "pinned host staging allocation failed");
     return bail(PSV_ENOMEM);
   }
@@ -686,6 +702,26 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
   if ((e = cudaMemsetAsync(ctx->arena, 0, L.total, ctx->stream)) != cudaSuccess) {
     cuda_fail(ctx, e, "arena clear");
     return bail(PSV_ECUDA);
+  }
+  // Timestep sinusoids of t_s = 1 - s/S, in f64: [cos(t f_j), sin(t f_j)],
+  // f_j = exp(-ln(1e4) j / (E/2)); shared by every stream and chunk table.
+  {
+    const int E = m.t_embed;
+    std::vector<float> emb(static_cast<size_t>(m.S) * E);
+    for (int s = 0; s < m.S; ++s) {
+      const double t = 1.0 - static_cast<double>(s) / m.S;
+      for (int j = 0; j < E / 2; ++j) {
+        const double f = std::exp(-std::log(1e4) * j / (E / 2));
+        emb[static_cast<size_t>(s) * E + j] = static_cast<float>(std::cos(t * f));
+        emb[static_cast<size_t>(s) * E + E / 2 + j] = static_cast<float>(std::sin(t * f));
+      }
+    }
+    if ((e = cudaMemcpyAsync(ctx->at<float>(L.temb_in), emb.data(), emb.size() * 4, cudaMemcpyHostToDevice,
+                             ctx->stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(ctx->stream)) != cudaSuccess) {
+      cuda_fail(ctx, e, "timestep table upload");
+      return bail(PSV_ECUDA);
+    }
   }
   // RoPE table of in-chunk offsets: (cos, sin) of i * theta^(-2j/dh), f64.
   {
@@ -873,6 +909,36 @@ static bool all_weights_loaded(const psv_ctx* ctx) {
   return true;
 }
 
+namespace {
+
+// adaLN tables of conditioning table `tab` (a stream, or max_streams + a
+// chunk slot) from the device vector cond [d]: for every step s,
+// e_s = W_t2 SiLU(W_t1 emb(t_s) + b_t1) + b_t2 + cond,
+// mod[tab][s] = W_mod SiLU(e_s) + b_mod (all blocks), fmod[tab][s] likewise.
+cudaError_t build_cond_tables(psv_ctx* ctx, const float* cond, int tab) {
+  const psv_model_desc& m = ctx->m;
+  const Layout& L = ctx->L;
+  const int S = m.S, E = m.t_embed, d = m.d;
+  float* s_a1 = ctx->at<float>(L.scratch);
+  float* s_e = s_a1 + static_cast<size_t>(8) * d;
+  cudaStream_t st = ctx->stream;
+  cudaError_t e;
+  if ((e = psv::launch_cond_linear(ctx->at<float>(L.temb_in), S, E, ctx->at<__nv_bfloat16>(L.w_t1),
+                                   ctx->at<float>(L.b_t1), nullptr, s_a1, d, 0, st)) != cudaSuccess)
+    return e;
+  if ((e = psv::launch_cond_linear(s_a1, S, d, ctx->at<__nv_bfloat16>(L.w_t2), ctx->at<float>(L.b_t2), cond, s_e,
+                                   d, 1, st)) != cudaSuccess)
+    return e;
+  if ((e = psv::launch_cond_linear(s_e, S, d, ctx->at<__nv_bfloat16>(L.w_mod), ctx->at<float>(L.b_mod), nullptr,
+                                   ctx->at<float>(L.mod) + static_cast<size_t>(tab) * S * m.B * 6 * d,
+                                   m.B * 6 * d, 1, st)) != cudaSuccess)
+    return e;
+  return psv::launch_cond_linear(s_e, S, d, ctx->at<__nv_bfloat16>(L.w_fmod), ctx->at<float>(L.b_fmod), nullptr,
+                                 ctx->at<float>(L.fmod) + static_cast<size_t>(tab) * S * 2 * d, 2 * d, 1, st);
+}
+
+}  // namespace
+
 PSV_API int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id) {
   if (int r = check_ctx(ctx)) return r;
   if (!stream_id || (!cond && !ctx->plan_only)) return set_err(ctx, PSV_EINVAL, "null argument");
@@ -884,37 +950,13 @@ PSV_API int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id) {
     if (!all_weights_loaded(ctx)) return set_err(ctx, PSV_EINVAL, "load every weight before opening a stream");
     const psv_model_desc& m = ctx->m;
     const Layout& L = ctx->L;
-    const int S = m.S, E = m.t_embed, d = m.d;
-    // Timestep sinusoids of t_s = 1 - s/S, in f64: [cos(t f_j), sin(t f_j)],
-    // f_j = exp(-ln(1e4) j / (E/2)).
-    float* emb = ctx->h_misc;
-    float* hc = ctx->h_misc + static_cast<size_t>(8) * E;
-    for (int s = 0; s < S; ++s) {
-      const double t = 1.0 - static_cast<double>(s) / S;
-      for (int j = 0; j < E / 2; ++j) {
-        const double f = std::exp(-std::log(1e4) * j / (E / 2));
-        emb[s * E + j] = static_cast<float>(std::cos(t * f));
-        emb[s * E + E / 2 + j] = static_cast<float>(std::sin(t * f));
-      }
-    }
-    std::memcpy(hc, cond, static_cast<size_t>(d) * 4);
-    float* s_emb = ctx->at<float>(L.scratch);
-    float* s_a1 = s_emb + static_cast<size_t>(8) * E;
-    float* s_e = s_a1 + static_cast<size_t>(8) * d;
-    float* s_cond = s_e + static_cast<size_t>(8) * d;
+    const int d = m.d;
     cudaStream_t st = ctx->stream;
-    CK(cudaMemcpyAsync(s_emb, emb, static_cast<size_t>(S) * E * 4, cudaMemcpyHostToDevice, st), "emb upload");
-    CK(cudaMemcpyAsync(s_cond, hc, static_cast<size_t>(d) * 4, cudaMemcpyHostToDevice, st), "cond upload");
-    CK(psv::launch_cond_linear(s_emb, S, E, ctx->at<__nv_bfloat16>(L.w_t1), ctx->at<float>(L.b_t1), nullptr, s_a1,
-                               d, 0, st), "time MLP 1");
-    CK(psv::launch_cond_linear(s_a1, S, d, ctx->at<__nv_bfloat16>(L.w_t2), ctx->at<float>(L.b_t2), s_cond, s_e, d,
-                               1, st), "time MLP 2");
-    CK(psv::launch_cond_linear(s_e, S, d, ctx->at<__nv_bfloat16>(L.w_mod), ctx->at<float>(L.b_mod), nullptr,
-                               ctx->at<float>(L.mod) + static_cast<size_t>(sid) * S * m.B * 6 * d, m.B * 6 * d, 1,
-                               st), "adaLN tables");
-    CK(psv::launch_cond_linear(s_e, S, d, ctx->at<__nv_bfloat16>(L.w_fmod), ctx->at<float>(L.b_fmod), nullptr,
-                               ctx->at<float>(L.fmod) + static_cast<size_t>(sid) * S * 2 * d, 2 * d, 1, st),
-       "final adaLN table");
+    std::memcpy(ctx->h_misc, cond, static_cast<size_t>(m.d) * 4);
+    float* s_cond = ctx->at<float>(L.scratch) + static_cast<size_t>(8) * (m.t_embed + 2 * m.d);
+    CK(cudaMemcpyAsync(s_cond, ctx->h_misc, static_cast<size_t>(m.d) * 4, cudaMemcpyHostToDevice, ctx->stream),
+       "cond upload");
+    CK(build_cond_tables(ctx, s_cond, sid), "adaLN tables");
     // Fresh rings: chunk 0 of the new stream must not see an old stream's keys
     // (it attends to slot 0 only, but masked tails must stay finite).
     const size_t ring_k = static_cast<size_t>(L.Lr) * d * 2, ring_v = static_cast<size_t>(d) * L.Lp * 2;
@@ -927,11 +969,29 @@ PSV_API int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id) {
   s = StreamState();
   s.open = true;
   s.finish_wave.assign(ctx->inflight, -1);
+  s.own_cond.assign(ctx->inflight, 0);
   *stream_id = sid;
   return PSV_OK;
 }
 
+namespace {
+int submit_impl(psv_ctx* ctx, int sid, const float* noise, const float* cond, bool with_cond);
+}  // namespace
+
 PSV_API int psv_submit_chunk(psv_ctx* ctx, int sid, const float* noise) {
+  return submit_impl(ctx, sid, noise, nullptr, false);
+}
+
+PSV_API int psv_submit_chunk_cond(psv_ctx* ctx, int sid, const float* noise, const float* cond) {
+  if (int r = check_ctx(ctx)) return r;
+  if (!(ctx->m.flags & PSV_FLAG_CHUNK_COND))
+    return set_err(ctx, PSV_EINVAL, "per-chunk conditioning needs a context created with PSV_FLAG_CHUNK_COND");
+  if (!cond && !ctx->plan_only) return set_err(ctx, PSV_EINVAL, "null cond");
+  return submit_impl(ctx, sid, noise, cond, true);
+}
+
+namespace {
+int submit_impl(psv_ctx* ctx, int sid, const float* noise, const float* cond, bool with_cond) {
   if (int r = check_ctx(ctx)) return r;
   if (sid < 0 || sid >= static_cast<int>(ctx->streams.size()) || !ctx->streams[sid].open)
     return set_err(ctx, PSV_EINVAL, "stream %d is not open", sid);
@@ -957,10 +1017,21 @@ PSV_API int psv_submit_chunk(psv_ctx* ctx, int sid, const float* noise) {
     CK(cudaMemcpyAsync(ctx->at<float2>(ctx->L.rope_base) + static_cast<size_t>(slot) * (m.dh / 2), rb,
                        static_cast<size_t>(m.dh / 2) * 8, cudaMemcpyHostToDevice, ctx->stream),
        "rope upload");
+    if (with_cond) {
+      // The slot's staging and table are free: its previous chunk was polled.
+      float* hc = ctx->h_ccond + static_cast<size_t>(slot) * m.d;
+      float* dc = ctx->at<float>(ctx->L.ccond) + static_cast<size_t>(slot) * m.d;
+      std::memcpy(hc, cond, static_cast<size_t>(m.d) * 4);
+      CK(cudaMemcpyAsync(dc, hc, static_cast<size_t>(m.d) * 4, cudaMemcpyHostToDevice, ctx->stream),
+         "chunk cond upload");
+      CK(build_cond_tables(ctx, dc, m.max_streams + slot), "chunk adaLN tables");
+    }
   }
+  s.own_cond[static_cast<size_t>(c % ctx->inflight)] = with_cond ? 1 : 0;
   s.n_sub += 1;
   return PSV_OK;
 }
+}  // namespace
 
 PSV_API int psv_wave_plan(psv_ctx* ctx, psv_task* buf, int cap, int* n) {
   if (!ctx || !n || cap < 0 || (cap > 0 && !buf)) return PSV_EINVAL;
@@ -1109,6 +1180,7 @@ PSV_API void psv_destroy(psv_ctx* ctx) {
     if (ctx->h_rope) cudaFreeHost(ctx->h_rope);
     if (ctx->h_out) cudaFreeHost(ctx->h_out);
     if (ctx->h_misc) cudaFreeHost(ctx->h_misc);
+    if (ctx->h_ccond) cudaFreeHost(ctx->h_ccond);
     if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
     if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   }

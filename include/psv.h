@@ -48,6 +48,8 @@ extern "C" {
 #define PSV_FLAG_PLAN_ONLY   1  /* host scheduler only: no device, no arena     */
 #define PSV_FLAG_SEQUENTIAL  2  /* one task per wave, lowest (stream, chunk,
                                    step) first: strictly sequential order       */
+#define PSV_FLAG_CHUNK_COND  4  /* reserve per-chunk conditioning tables, for
+                                   psv_submit_chunk_cond                       */
 
 /* ---- model description --------------------------------------------------
  * B blocks, S Euler steps (t_s = 1 - s/S), model width d = H*dh, MLP width
@@ -113,6 +115,9 @@ typedef struct psv_task {
   int32_t kv_len;      /* keys the task attends to: (min(c, W) + 1) * T      */
   int32_t row_off;     /* first row of the task in the wave's batch          */
   int32_t state_slot;  /* latent state slot holding x of this chunk          */
+  int32_t cond_table;  /* adaLN tables the task reads: its stream id, or
+                          max_streams + state_slot for a chunk submitted with
+                          its own conditioning (psv_submit_chunk_cond)       */
 } psv_task;
 
 /* Per-kernel timing, filled when profiling is on (psv_set_profiling). */
@@ -155,6 +160,18 @@ int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id);
  * x_0).  Chunks are numbered 0, 1, ... in submission order.  Errors:
  * PSV_EAGAIN (max_inflight chunks alive: poll first), PSV_EINVAL. */
 int psv_submit_chunk(psv_ctx* ctx, int stream_id, const float* noise);
+
+/* Submit the next chunk with its own conditioning vector cond (host, f32
+ * [d]): an action / observation embedding for this chunk only.  Every step
+ * of the chunk uses e_s = temb(t_s) + cond in place of the stream's vector
+ * (the pages' action-conditioned world models condition each generated
+ * chunk on the agent's action: AREX article, section 难题; BAAI
+ * announcement, section 新一代物理 AI 的基础设施).  The chunk's adaLN tables are
+ * built on the device before this call returns (asynchronously on the
+ * context stream, ahead of any later wave).  Needs a context created with
+ * PSV_FLAG_CHUNK_COND.  Errors: PSV_EINVAL (flag missing, null argument),
+ * PSV_EAGAIN (max_inflight chunks alive), PSV_ECUDA. */
+int psv_submit_chunk_cond(psv_ctx* ctx, int stream_id, const float* noise, const float* cond);
 
 /* Run one wave: every task whose dependencies are met, all streams batched
  * block by block.  Asynchronous on the context stream.  *n_tasks = tasks

@@ -34,7 +34,10 @@ Readings where the definition is open are marked ``reading <n>``:
   <8> RoPE rotates interleaved pairs (2j, 2j+1) by pos * theta^(-2j/dh);
   <9> no mask: a chunk is bidirectional and its whole window is visible;
   <10> softmax scale 1/sqrt(dh);
-  <11> GELU is the tanh approximation.
+  <11> GELU is the tanh approximation;
+  <18> a chunk submitted with its own conditioning vector (an action /
+       observation embedding) uses it in place of the stream's at every
+       step of that chunk: e_s = temb(t_s) + cond_chunk (``runner.submit``).
 """
 from __future__ import annotations
 

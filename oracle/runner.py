@@ -24,6 +24,7 @@ class OracleStream:
         self.step = {}     # chunk -> next step to run
         self.kv = {}       # (b, s, c) -> (k, v)
         self.outputs = {}  # chunk -> x_S
+        self.chunk_mod = {}  # chunk -> (mod, fmod) of a chunk submitted with its own cond
         self.n_submitted = 0
 
 
@@ -44,9 +45,16 @@ class OracleRunner:
         self.streams.append(OracleStream(self, cond))
         return self.sim.open_stream()
 
-    def submit(self, sid: int, noise: np.ndarray):
+    def submit(self, sid: int, noise: np.ndarray, cond: np.ndarray | None = None):
+        """Next chunk of stream sid.  ``cond`` gives this chunk its own
+        conditioning vector, used at every step of the chunk in place of the
+        stream's (reading <18>: an action-conditioned world model conditions
+        each generated chunk on the agent's action — AREX article, section
+        难题; BAAI announcement, section 新一代物理 AI 的基础设施)."""
         st = self.streams[sid]
         c = st.n_submitted
+        if cond is not None:
+            st.chunk_mod[c] = M.conditioning(self.cfg, self.g, self.blocks, cond, self.dtype)
         st.x[c] = noise.reshape(self.cfg["T"], self.cfg["C"]).astype(self.dtype)
         st.step[c] = 0
         st.n_submitted += 1
@@ -61,20 +69,22 @@ class OracleRunner:
         assert st.step[c] == s, "task run out of order"
         W = cfg["W"]
         pos = M.positions(cfg, c)
+        mod, fmod = st.chunk_mod.get(c, (st.mod, st.fmod))
         h = M.in_proj(self.g, st.x[c])
         for b in range(cfg["B"]):
             window = [st.kv[(b, s, cc)] for cc in range(max(0, c - W), c)]
-            h_out, k, v = M.block_forward(cfg, self.blocks[b], st.mod[s, b], h, pos, window)
+            h_out, k, v = M.block_forward(cfg, self.blocks[b], mod[s, b], h, pos, window)
             if tap is not None:
                 tap(b, h, h_out)
             st.kv[(b, s, c)] = (k, v)
             st.kv.pop((b, s, c - W - 1), None)
             h = h_out
-        vel = M.final_velocity(cfg, self.g, st.fmod[s], h)
+        vel = M.final_velocity(cfg, self.g, fmod[s], h)
         st.x[c] = M.euler(st.x[c], vel, self.ts[s], self.ts[s + 1])
         st.step[c] = s + 1
         if s + 1 == cfg["S"]:
             st.outputs[c] = st.x.pop(c)
+            st.chunk_mod.pop(c, None)
         self.task_log.append((sid, c, s))
 
     def run_wave(self) -> list:

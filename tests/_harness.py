@@ -30,9 +30,10 @@ def gpu_session(cfg, weights, n_streams, flags=0, max_inflight=0):
     return s
 
 
-def run_gpu(cfg, weights, streams, n_chunks, flags=0, conds=None, noises=None):
+def run_gpu(cfg, weights, streams, n_chunks, flags=0, conds=None, noises=None, chunk_conds=None):
     """outputs[sid][c] of a full run: every chunk submitted up front, waves
-    until idle, then every chunk polled."""
+    until idle, then every chunk polled.  chunk_conds[sid] = {c: vector}
+    submits those chunks with their own conditioning."""
     n_streams = len(streams)
     sess = gpu_session(cfg, weights, n_streams, flags, max_inflight=n_chunks + cfg["S"])
     try:
@@ -41,7 +42,9 @@ def run_gpu(cfg, weights, streams, n_chunks, flags=0, conds=None, noises=None):
             assert sid == i
             for c in range(n_chunks):
                 x0 = st.noise(c) if noises is None else noises[i][c]
-                sess.submit(sid, np.ascontiguousarray(x0, dtype=np.float32))
+                cc = None if chunk_conds is None else chunk_conds[i].get(c)
+                sess.submit(sid, np.ascontiguousarray(x0, dtype=np.float32),
+                            None if cc is None else np.ascontiguousarray(cc, dtype=np.float32))
         waves = 0
         while sess.run_wave():
             waves += 1
@@ -60,11 +63,13 @@ def run_gpu(cfg, weights, streams, n_chunks, flags=0, conds=None, noises=None):
         sess.close()
 
 
-def run_oracle(cfg, weights, streams, n_chunks, dtype=np.float64, conds=None, noises=None):
+def run_oracle(cfg, weights, streams, n_chunks, dtype=np.float64, conds=None, noises=None,
+               chunk_conds=None):
     r = OracleRunner(cfg, weights, dtype)
     for i, st in enumerate(streams):
         r.open_stream(st.cond if conds is None else conds[i])
         for c in range(n_chunks):
-            r.submit(i, st.noise(c) if noises is None else noises[i][c])
+            r.submit(i, st.noise(c) if noises is None else noises[i][c],
+                     cond=None if chunk_conds is None else chunk_conds[i].get(c))
     r.run_until_idle()
     return [[r.streams[i].outputs[c] for c in range(n_chunks)] for i in range(len(streams))]

@@ -184,3 +184,39 @@ def test_create_rejects_small_arena_without_device():
     with pytest.raises(P.PSVError) as e:
         P.psv_create(P.model_desc(cfg), 0, 0, 0)
     assert e.value.code in (P.PSV_EINVAL, P.PSV_ENOMEM)
+
+
+def test_chunk_conditioning_tables_in_plan():
+    """A chunk submitted with its own conditioning reads table
+    max_streams + state_slot at every step; the others read their stream's.
+    Without PSV_FLAG_CHUNK_COND the call is refused, and the flag grows the
+    arena by one table set per chunk slot."""
+    cfg = synth.config("tiny")
+    ctx = _plan_ctx(cfg, 2, P.PSV_FLAG_CHUNK_COND, max_inflight=8)
+    s0 = P.psv_open_stream(ctx, None)
+    s1 = P.psv_open_stream(ctx, None)
+    P.psv_submit_chunk(ctx, s0, None)
+    P.psv_submit_chunk_cond(ctx, s0, None, None)
+    P.psv_submit_chunk_cond(ctx, s1, None, None)
+    seen = {}
+    while True:
+        plan = P.psv_wave_plan(ctx, cond_tables=True)
+        if not plan:
+            break
+        for (sid, c, s, slot, kv, row, state_slot, tab) in plan:
+            want = sid if (sid, c) == (s0, 0) else 2 + state_slot
+            assert tab == want, (sid, c, s, tab)
+            seen[(sid, c, s)] = tab
+        P.psv_run_wave(ctx)
+    assert len(seen) == 3 * cfg["S"]
+    P.psv_destroy(ctx)
+    ctx = _plan_ctx(cfg, 1)
+    sid = P.psv_open_stream(ctx, None)
+    with pytest.raises(P.PSVError) as e:
+        P.psv_submit_chunk_cond(ctx, sid, None, None)
+    assert e.value.code == P.PSV_EINVAL
+    P.psv_destroy(ctx)
+    base = P.psv_arena_bytes(P.model_desc(cfg, 2, 8))
+    more = P.psv_arena_bytes(P.model_desc(cfg, 2, 8, P.PSV_FLAG_CHUNK_COND))
+    per_slot = cfg["S"] * (cfg["B"] * 6 + 2) * cfg["d"] * 4  # mod + fmod tables of one slot
+    assert more - base >= 16 * per_slot

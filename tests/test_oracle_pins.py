@@ -385,3 +385,56 @@ def test_fp32_oracle_close_to_fp64():
         outs[dt] = np.stack([r.streams[0].outputs[c] for c in range(cfg["n_chunks"])])
     x64, x32 = outs[np.float64], outs[np.float32].astype(np.float64)
     assert np.linalg.norm(x32 - x64) / np.linalg.norm(x64) < 1e-5
+
+
+def test_chunk_conditioning_matches_stream_conditioning():
+    """Per-chunk conditioning (reading <18>) with W = 0: chunk 2 of a stream,
+    submitted with its own vector a, equals chunk 0 of a stream opened with a
+    (same noise; RoPE scores depend on position differences only), while the
+    neighbouring chunks keep the stream's vector."""
+    cfg = _tiny_cfg(W=0)
+    w = synth.make_weights(cfg, 0)
+    st = synth.make_streams(cfg, 1)[0]
+    a = np.random.default_rng(7).standard_normal(cfg["d"]).astype(np.float32)
+    r = OracleRunner(cfg, w)
+    r.open_stream(st.cond)
+    r.open_stream(a)
+    r.open_stream(st.cond)
+    r.submit(0, st.noise(0))
+    r.submit(0, st.noise(1))
+    r.submit(0, st.noise(2), cond=a)
+    r.submit(0, st.noise(3))
+    r.submit(1, st.noise(2))
+    r.submit(2, st.noise(3))
+    r.run_until_idle()
+    assert np.max(np.abs(r.streams[0].outputs[2] - r.streams[1].outputs[0])) < 1e-9
+    # chunk 3 went back to the stream's vector
+    assert np.max(np.abs(r.streams[0].outputs[3] - r.streams[2].outputs[0])) < 1e-9
+
+
+def test_chunk_conditioning_is_causal():
+    """With W > 0 a chunk's vector reaches later chunks only through its
+    stored KV: chunks before it are bit-identical, it and later ones change;
+    a vector equal to the stream's gives the unconditioned run bit for bit."""
+    cfg = _tiny_cfg()
+    w = synth.make_weights(cfg, 0)
+    st = synth.make_streams(cfg, 1)[0]
+    a = np.random.default_rng(8).standard_normal(cfg["d"]).astype(np.float32)
+
+    def run(conds):
+        r = OracleRunner(cfg, w)
+        r.open_stream(st.cond)
+        for c in range(5):
+            r.submit(0, st.noise(c), cond=conds.get(c))
+        r.run_until_idle()
+        return r.streams[0].outputs
+
+    base = run({})
+    same = run({2: st.cond})
+    moved = run({2: a})
+    for c in range(5):
+        assert np.array_equal(base[c], same[c])
+    for c in (0, 1):
+        assert np.array_equal(base[c], moved[c])
+    for c in (2, 3, 4):
+        assert np.max(np.abs(base[c] - moved[c])) > 1e-6

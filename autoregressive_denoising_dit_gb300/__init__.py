@@ -54,6 +54,17 @@ class Session:
     def open_stream(self, cond):
         return _psv.psv_open_stream(self.ctx, cond)
 
+    def admit_stream(self, cond, slo_ms: float = 0.0):
+        """Open a stream under admission control: (stream id, predicted ms per
+        chunk), or PSVError (code PSV_EAGAIN) if it is rejected."""
+        return _psv.psv_admit_stream(self.ctx, cond, slo_ms)
+
+    def close_stream(self, sid):
+        _psv.psv_close_stream(self.ctx, sid)
+
+    def predict_wave_ms(self, n_streams: int) -> float:
+        return _psv.psv_predict_wave_ms(self.ctx, n_streams)
+
     def submit(self, sid, noise, cond=None):
         """Submit the stream's next chunk; ``cond`` [d] gives the chunk its own
         conditioning vector (needs ``flags`` with PSV_FLAG_CHUNK_COND)."""

@@ -43,7 +43,8 @@ WEIGHT_IDS = {
 EXPORTS = [
     "psv_arena_bytes", "psv_create", "psv_load_weights", "psv_open_stream",
     "psv_submit_chunk", "psv_submit_chunk_cond", "psv_run_wave", "psv_poll_chunk", "psv_sync",
-    "psv_wave_plan", "psv_close_stream", "psv_destroy", "psv_last_error",
+    "psv_wave_plan", "psv_close_stream", "psv_predict_wave_ms", "psv_admit_stream",
+    "psv_destroy", "psv_last_error",
     "psv_set_graphs", "psv_set_profiling", "psv_kernel_times", "psv_debug_tap",
     "psv_debug_read_kv", "psv_attention_scratch_bytes", "psv_attention",
     "psv_attention_noalloc",
@@ -112,6 +113,9 @@ def lib() -> ctypes.CDLL:
             "psv_sync": (i32, [vp, i32]),
             "psv_wave_plan": (i32, [vp, ctypes.POINTER(Task), i32, ctypes.POINTER(i32)]),
             "psv_close_stream": (i32, [vp, i32]),
+            "psv_predict_wave_ms": (i32, [vp, i32, ctypes.POINTER(ctypes.c_double)]),
+            "psv_admit_stream": (i32, [vp, vp, ctypes.c_double, ctypes.POINTER(i32),
+                                       ctypes.POINTER(ctypes.c_double)]),
             "psv_destroy": (None, [vp]),
             "psv_last_error": (ctypes.c_char_p, [vp]),
             "psv_set_graphs": (i32, [vp, i32]),
@@ -238,6 +242,27 @@ def psv_wave_plan(ctx, cond_tables: bool = False) -> list:
     if cond_tables:
         return [buf[i].as_tuple() + (buf[i].cond_table,) for i in range(n.value)]
     return [buf[i].as_tuple() for i in range(n.value)]
+
+
+def psv_predict_wave_ms(ctx, n_streams: int) -> float:
+    ms = ctypes.c_double()
+    _check(ctx, lib().psv_predict_wave_ms(ctx, n_streams, ctypes.byref(ms)))
+    return ms.value
+
+
+def psv_admit_stream(ctx, cond: np.ndarray | None, slo_ms: float) -> tuple:
+    """(stream id, predicted ms per chunk); PSVError with code PSV_EAGAIN when
+    the stream is rejected (its .predicted_ms holds the prediction)."""
+    sid = ctypes.c_int()
+    pred = ctypes.c_double(float("nan"))
+    ptr = None if cond is None else _fptr(cond)
+    r = lib().psv_admit_stream(ctx, ptr, float(slo_ms), ctypes.byref(sid), ctypes.byref(pred))
+    try:
+        _check(ctx, r)
+    except PSVError as e:
+        e.predicted_ms = pred.value
+        raise
+    return sid.value, pred.value
 
 
 def psv_close_stream(ctx, sid: int) -> None:

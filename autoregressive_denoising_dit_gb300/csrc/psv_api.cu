@@ -236,6 +236,19 @@ struct StreamState {
   int64_t done[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   std::vector<int64_t> finish_wave;  // per state slot: wave that finished the chunk
   std::vector<char> own_cond;        // per state slot: chunk submitted with its own cond
+  double slo_ms = 0.0;               // SLO the stream was admitted with (0: none)
+};
+
+// Device-timed waves, for the admission model.
+struct WaveTiming {
+  cudaEvent_t t0 = nullptr, t1 = nullptr;
+  int n_tasks = 0;
+  bool full = false;    // every task had a full window (a steady wave)
+  bool pending = false;
+};
+struct WaveStat {
+  int64_t count = 0;
+  double mean_ms = 0.0;
 };
 
 struct ProfRec {
@@ -274,6 +287,8 @@ struct psv_ctx {
   float* h_ccond = nullptr;   // [n_slots][d] per-chunk conditioning staging
   size_t h_misc_bytes = 0;
   cudaEvent_t wave_ev[kWaveEvents] = {};
+  WaveTiming wave_tm[kWaveEvents];
+  std::map<int, WaveStat> wave_stats;  // task count -> steady wave time
   // tensor maps
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
   CUtensorMap tmC_h;  // f32 h, the target of the gated-residual TMA reductions
@@ -696,7 +711,11 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
     return bail(PSV_ENOMEM);
   }
   for (int i = 0; i < kTaskBufs; ++i) cudaEventCreateWithFlags(&ctx->task_ev[i], cudaEventDisableTiming);
-  for (int i = 0; i < kWaveEvents; ++i) cudaEventCreateWithFlags(&ctx->wave_ev[i], cudaEventDisableTiming);
+  for (int i = 0; i < kWaveEvents; ++i) {
+    cudaEventCreateWithFlags(&ctx->wave_ev[i], cudaEventDisableTiming);
+    cudaEventCreate(&ctx->wave_tm[i].t0);
+    cudaEventCreate(&ctx->wave_tm[i].t1);
+  }
   // Zero the whole arena: padded weight rows, rings (masked keys must be
   // finite), activations, tables and the error word.
   if ((e = cudaMemsetAsync(ctx->arena, 0, L.total, ctx->stream)) != cudaSuccess) {
@@ -1042,6 +1061,78 @@ PSV_API int psv_wave_plan(psv_ctx* ctx, psv_task* buf, int cap, int* n) {
   return PSV_OK;
 }
 
+namespace {
+
+// Fold every finished, timed steady wave into the per-task-count means.
+void harvest_wave_times(psv_ctx* ctx) {
+  for (WaveTiming& tm : ctx->wave_tm) {
+    if (!tm.pending) continue;
+    if (cudaEventQuery(tm.t1) != cudaSuccess) continue;
+    tm.pending = false;
+    float ms = 0.0f;
+    if (!tm.full || cudaEventElapsedTime(&ms, tm.t0, tm.t1) != cudaSuccess) continue;
+    WaveStat& w = ctx->wave_stats[tm.n_tasks];
+    w.count += 1;
+    w.mean_ms += (ms - w.mean_ms) / static_cast<double>(w.count);
+  }
+}
+
+// Algorithmic FLOPs of a steady wave with n tasks (full windows): the block
+// GEMMs, the window attention, the in-projection and the velocity head.
+double steady_wave_flops(const psv_model_desc& m, int n) {
+  const double T = m.T, d = m.d, F = m.F, C = m.C, B = m.B, Lk = static_cast<double>(m.W + 1) * m.T;
+  const double per_task = 2.0 * T * B * (4.0 * d * d + 2.0 * d * F) + 4.0 * T * Lk * d * B + 4.0 * T * C * d;
+  return per_task * n;
+}
+
+double predict_wave_ms(psv_ctx* ctx, int n_streams) {
+  if (!ctx->plan_only) harvest_wave_times(ctx);
+  const int n = n_streams * ctx->m.S;
+  auto hit = ctx->wave_stats.find(n);
+  if (hit != ctx->wave_stats.end() && hit->second.count > 0) return hit->second.mean_ms;
+  int best = -1;
+  for (const auto& kv : ctx->wave_stats)
+    if (kv.second.count > 0 && (best < 0 || std::abs(kv.first - n) < std::abs(best - n))) best = kv.first;
+  if (best > 0)
+    return ctx->wave_stats[best].mean_ms * steady_wave_flops(ctx->m, n) / steady_wave_flops(ctx->m, best);
+  constexpr double kUnmeasuredFlops = 1.0e15;  // 1 PFLOP/s until a wave was timed
+  return steady_wave_flops(ctx->m, n) / kUnmeasuredFlops * 1e3;
+}
+
+}  // namespace
+
+PSV_API int psv_predict_wave_ms(psv_ctx* ctx, int n_streams, double* ms) {
+  if (int r = check_ctx(ctx)) return r;
+  if (!ms || n_streams < 1 || n_streams > ctx->m.max_streams)
+    return set_err(ctx, PSV_EINVAL, "need 1 <= n_streams <= %d", ctx->m.max_streams);
+  *ms = predict_wave_ms(ctx, n_streams);
+  return PSV_OK;
+}
+
+PSV_API int psv_admit_stream(psv_ctx* ctx, const float* cond, double slo_ms, int* stream_id,
+                             double* predicted_ms) {
+  if (int r = check_ctx(ctx)) return r;
+  if (!stream_id) return set_err(ctx, PSV_EINVAL, "null stream_id");
+  int n_open = 0;
+  for (const StreamState& s : ctx->streams) n_open += s.open ? 1 : 0;
+  if (n_open >= ctx->m.max_streams)
+    return set_err(ctx, PSV_EAGAIN, "rejected: no KV ring set free (%d streams open)", n_open);
+  const double pred = predict_wave_ms(ctx, n_open + 1);
+  if (predicted_ms) *predicted_ms = pred;
+  if (slo_ms > 0.0 && pred > slo_ms)
+    return set_err(ctx, PSV_EAGAIN, "rejected: predicted %.3f ms per chunk > the stream's SLO %.3f ms", pred,
+                   slo_ms);
+  for (int i = 0; i < static_cast<int>(ctx->streams.size()); ++i) {
+    const StreamState& s = ctx->streams[i];
+    if (s.open && s.slo_ms > 0.0 && pred > s.slo_ms)
+      return set_err(ctx, PSV_EAGAIN, "rejected: predicted %.3f ms per chunk > stream %d's SLO %.3f ms", pred, i,
+                     s.slo_ms);
+  }
+  if (int r = psv_open_stream(ctx, cond, stream_id)) return r;
+  ctx->streams[*stream_id].slo_ms = slo_ms > 0.0 ? slo_ms : 0.0;
+  return PSV_OK;
+}
+
 PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
   if (int r = check_ctx(ctx)) return r;
   if (!n_tasks) return set_err(ctx, PSV_EINVAL, "null n_tasks");
@@ -1051,6 +1142,13 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
   *n_tasks = n;
   if (n == 0) return PSV_OK;
   if (!ctx->plan_only) {
+    harvest_wave_times(ctx);
+    WaveTiming& tm = ctx->wave_tm[ctx->wave_id % kWaveEvents];
+    if (tm.pending) {
+      // The slot's previous wave is 64 waves old; make sure it was counted.
+      CK(cudaEventSynchronize(tm.t1), "wave timing");
+      harvest_wave_times(ctx);
+    }
     std::vector<TaskDev> dev(n);
     for (int i = 0; i < n; ++i) dev[i] = to_dev(ctx, tasks[i]);
     // Task table: pinned ring buffer, reused only after its copy finished.
@@ -1062,6 +1160,10 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
     CK(cudaMemcpyAsync(ctx->at<TaskDev>(ctx->L.tasks), h, sizeof(TaskDev) * n, cudaMemcpyHostToDevice, ctx->stream),
        "task table upload");
     CK(cudaEventRecord(ctx->task_ev[tb], ctx->stream), "task event");
+    tm.n_tasks = n;
+    tm.full = true;
+    for (const TaskDev& t : dev) tm.full = tm.full && t.kv_len == ctx->L.Lr;
+    CK(cudaEventRecord(tm.t0, ctx->stream), "wave timing");
     const bool tap = ctx->tap_block >= 0;
     const bool eager = ctx->profiling || tap || !ctx->use_graphs;
     if (eager) {
@@ -1099,6 +1201,10 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
       seen += 1;
     }
     CK(cudaEventRecord(ctx->wave_ev[ctx->wave_id % kWaveEvents], ctx->stream), "wave event");
+    CK(cudaEventRecord(tm.t1, ctx->stream), "wave timing");
+    // Profiled and tapped waves run eagerly with extra synchronisation: not
+    // representative of the steady state.
+    tm.pending = !eager;
   }
   for (const psv_task& t : tasks) {
     StreamState& s = ctx->streams[t.stream];
@@ -1175,6 +1281,10 @@ PSV_API void psv_destroy(psv_ctx* ctx) {
       if (ctx->task_ev[i]) cudaEventDestroy(ctx->task_ev[i]);
     for (int i = 0; i < kWaveEvents; ++i)
       if (ctx->wave_ev[i]) cudaEventDestroy(ctx->wave_ev[i]);
+    for (int i = 0; i < kWaveEvents; ++i) {
+      if (ctx->wave_tm[i].t0) cudaEventDestroy(ctx->wave_tm[i].t0);
+      if (ctx->wave_tm[i].t1) cudaEventDestroy(ctx->wave_tm[i].t1);
+    }
     if (ctx->h_tasks) cudaFreeHost(ctx->h_tasks);
     if (ctx->h_noise) cudaFreeHost(ctx->h_noise);
     if (ctx->h_rope) cudaFreeHost(ctx->h_rope);

@@ -197,6 +197,33 @@ int psv_wave_plan(psv_ctx* ctx, psv_task* buf, int cap, int* n);
  * cancelled: call after its chunks were polled. */
 int psv_close_stream(psv_ctx* ctx, int stream_id);
 
+/* ---- admission control (one GPU) -----------------------------------------
+ * The pages admit a new stream only when the whole stream fits and its
+ * service objective (SLO) can be met, never migrate running streams, and so
+ * keep the service of the streams already admitted stable (AREX article,
+ * section 三层设计, third layer; BAAI announcement, section PhysisServe,
+ * multi-stream scheduling).  On one GPU: a stream's state is its KV rings
+ * (one of the max_streams ring sets reserved at create), and in steady state
+ * every open stream gets one chunk per wave, so every stream's ms per chunk
+ * is the shared wave time, which a new stream lengthens for all of them.
+ *
+ * Predicted steady wave time with n open streams (n*S tasks, full windows).
+ * The library times every wave on the device and keeps the mean of the
+ * full-window waves per task count; a count measured before is predicted by
+ * its mean, another one from the nearest measured count in proportion to
+ * the algorithmic FLOPs, and with no measurement at all from the
+ * algorithmic FLOPs at 1 PFLOP/s.  Errors: PSV_EINVAL (n < 1 or >
+ * max_streams). */
+int psv_predict_wave_ms(psv_ctx* ctx, int n_streams, double* ms);
+
+/* Open a stream (as psv_open_stream) only if a ring set is free and the
+ * predicted wave time with it meets slo_ms (ms per chunk, <= 0: none) and the
+ * SLO every open stream was admitted with.  *predicted_ms (may be NULL) gets
+ * the prediction.  Errors: PSV_EAGAIN (rejected: no ring set free, or an SLO
+ * would be missed; the reason is in psv_last_error), PSV_EINVAL, PSV_ECUDA. */
+int psv_admit_stream(psv_ctx* ctx, const float* cond, double slo_ms, int* stream_id,
+                     double* predicted_ms);
+
 /* Destroy the context (synchronises the stream first).  NULL is a no-op. */
 void psv_destroy(psv_ctx* ctx);
 

@@ -220,3 +220,44 @@ def test_chunk_conditioning_tables_in_plan():
     more = P.psv_arena_bytes(P.model_desc(cfg, 2, 8, P.PSV_FLAG_CHUNK_COND))
     per_slot = cfg["S"] * (cfg["B"] * 6 + 2) * cfg["d"] * 4  # mod + fmod tables of one slot
     assert more - base >= 16 * per_slot
+
+
+def _steady_flops(cfg, n_tasks):
+    T, d, F, C, B = cfg["T"], cfg["d"], cfg["F"], cfg["C"], cfg["B"]
+    Lk = (cfg["W"] + 1) * T
+    return n_tasks * (2 * T * B * (4 * d * d + 2 * d * F) + 4 * T * Lk * d * B + 4 * T * C * d)
+
+
+def test_admission_control_without_measurements():
+    """Admission (one GPU, no migration): a stream is admitted only while a KV
+    ring set is free and the predicted shared wave time meets its SLO and
+    every admitted stream's SLO.  Without timed waves the prediction is the
+    steady wave's algorithmic FLOPs at 1 PFLOP/s."""
+    cfg = synth.config("tiny")
+    ctx = _plan_ctx(cfg, 3)
+    p1 = P.psv_predict_wave_ms(ctx, 1)
+    assert abs(p1 - _steady_flops(cfg, cfg["S"]) / 1e15 * 1e3) < 1e-12 * max(1.0, p1)
+    assert abs(P.psv_predict_wave_ms(ctx, 3) - 3 * p1) < 1e-9 * p1
+    with pytest.raises(P.PSVError):
+        P.psv_predict_wave_ms(ctx, 4)
+    # the stream's own SLO
+    with pytest.raises(P.PSVError) as e:
+        P.psv_admit_stream(ctx, None, 0.5 * p1)
+    assert e.value.code == P.PSV_EAGAIN and "SLO" in str(e.value)
+    a, pa = P.psv_admit_stream(ctx, None, 2.0 * p1)      # tight: fits two streams
+    assert abs(pa - p1) < 1e-9 * p1
+    b, pb = P.psv_admit_stream(ctx, None, 0.0)           # no SLO of its own
+    assert abs(pb - 2 * p1) < 1e-9 * p1
+    with pytest.raises(P.PSVError) as e:                  # would break stream a's SLO
+        P.psv_admit_stream(ctx, None, 0.0)
+    assert e.value.code == P.PSV_EAGAIN and f"stream {a}" in str(e.value)
+    P.psv_close_stream(ctx, b)
+    c, pc = P.psv_admit_stream(ctx, None, 10 * p1)       # the freed ring set
+    assert c == b and abs(pc - 2 * p1) < 1e-9 * p1
+    P.psv_destroy(ctx)
+    ctx = _plan_ctx(cfg, 1)
+    P.psv_admit_stream(ctx, None, 0.0)
+    with pytest.raises(P.PSVError) as e:
+        P.psv_admit_stream(ctx, None, 0.0)
+    assert e.value.code == P.PSV_EAGAIN and "ring" in str(e.value)
+    P.psv_destroy(ctx)

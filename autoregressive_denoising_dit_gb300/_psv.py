@@ -25,6 +25,7 @@ PSV_EDEVICE = -6
 PSV_FLAG_PLAN_ONLY = 1
 PSV_FLAG_SEQUENTIAL = 2
 PSV_FLAG_CHUNK_COND = 4
+PSV_FLAG_LATENCY = 8
 
 PSV_DTYPE_F32 = 0
 PSV_DTYPE_BF16 = 1

@@ -264,6 +264,7 @@ struct psv_ctx {
   Layout L{};
   bool plan_only = false;
   bool sequential = false;
+  bool latency = false;
   cudaStream_t stream = nullptr;
   cudaStream_t copy_stream = nullptr;
   cudaStream_t cap_stream = nullptr;  // private stream graphs are captured on
@@ -368,6 +369,19 @@ void plan_wave(const psv_ctx* ctx, std::vector<psv_task>* out) {
       t.cond_table = st.own_cond[static_cast<size_t>(c % ctx->inflight)] ? m.max_streams + t.state_slot : sid;
       out->push_back(t);
     }
+  }
+  if (ctx->latency && !out->empty()) {
+    // Latency mode: each stream's oldest ready chunk only (tasks are grouped
+    // by stream, steps ascending; the oldest chunk has the lowest index).
+    std::vector<psv_task> keep;
+    for (const psv_task& t : *out) {
+      if (!keep.empty() && keep.back().stream == t.stream) {
+        if (t.chunk < keep.back().chunk) keep.back() = t;
+      } else {
+        keep.push_back(t);
+      }
+    }
+    out->swap(keep);
   }
   if (ctx->sequential && out->size() > 1) {
     auto best = std::min_element(out->begin(), out->end(), [](const psv_task& a, const psv_task& b) {
@@ -657,6 +671,7 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
   ctx->inflight = inflight_of(*desc);
   ctx->plan_only = (desc->flags & PSV_FLAG_PLAN_ONLY) != 0;
   ctx->sequential = (desc->flags & PSV_FLAG_SEQUENTIAL) != 0;
+  ctx->latency = (desc->flags & PSV_FLAG_LATENCY) != 0;
   ctx->blk_loaded.assign(static_cast<size_t>(desc->B) * 16, 0);
   ctx->streams.resize(desc->max_streams);
   for (auto& s : ctx->streams) s.finish_wave.assign(ctx->inflight, -1);

@@ -415,6 +415,8 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s / e2e_steps * 1e3},
         "gpu_launches": (3 + 7 * cfg["B"]) * args.steps,
         "clocks": clk,
+        # a chunk's S steps run in S consecutive steady waves
+        "response_ms": S * ms_step,
     }
     sess.close()
     if rank == 0 and not args.no_cpu_baseline:
@@ -424,6 +426,91 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
             "kind": "oracle",
             "sample": (f"f32 numpy oracle on {nb} transformer block(s) of one steady "
                        f"{n_task}-task wave, scaled x{cfg['B'] / nb:.1f} to the whole wave")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_latency(args, cfg_name, cfg, world, rank, local):
+    """Latency-mode schedule (PSV_FLAG_LATENCY): a wave runs each stream's
+    oldest ready chunk only, so a chunk's S steps run in S consecutive waves
+    of one task per stream.  Reports chunks/s over all streams, the response
+    time (first step to output: S such waves, device-timed) and the same
+    end to end through host buffers (submit a chunk, run its S waves, poll
+    it)."""
+    import torch
+
+    from autoregressive_denoising_dit_gb300 import Session, _psv as P
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    S, T, C = cfg["S"], cfg["T"], cfg["C"]
+    n_st = cfg["n_streams"]
+    n_chunks = args.warmup + args.steps
+    sess = Session(cfg, max_streams=n_st, max_inflight=n_chunks + args.steps + S + 8,
+                   flags=P.PSV_FLAG_LATENCY)
+    sess.load_device_weights(synth.iter_device_weights(cfg, seed=0, device=f"cuda:{local}"))
+    torch.cuda.synchronize()
+    streams = synth.make_streams(cfg)
+    sids = [sess.open_stream(st.cond) for st in streams]
+    for c in range(n_chunks):
+        for st, sid in zip(streams, sids):
+            sess.submit(sid, st.noise(c))
+    for _ in range(S * args.warmup):
+        sess.run_wave()
+    sess.sync(600000)
+    stream = sess.torch_stream
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(S * args.steps):
+        n = sess.run_wave()
+        assert n == n_st, f"latency-mode wave ran {n} tasks"
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms_chunk = total_ms / args.steps          # per stream: one chunk every S waves
+    buf = np.empty((T, C), dtype=np.float32)
+    for sid in sids:
+        while sess.poll(sid, buf) is not None:
+            pass
+    # end to end: submit one chunk per stream, run its S waves, poll it
+    next_chunk = n_chunks
+    e2e = []
+    for k in range(args.steps + 2):
+        w0 = time.perf_counter()
+        for st, sid in zip(streams, sids):
+            sess.submit(sid, st.noise(next_chunk))
+        for _ in range(S):
+            sess.run_wave()
+        for sid in sids:
+            while sess.poll(sid, buf) is None:
+                pass
+        if k >= 2:
+            e2e.append((time.perf_counter() - w0) * 1e3)
+        next_chunk += 1
+    e2e_ms = max_over_ranks(float(np.mean(e2e)), world, dev)
+    line = {
+        "metric": METRIC + " (latency-mode schedule)", "value": world * n_st / (ms_chunk / 1e3),
+        "unit": "chunks/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_chunk, "ms_per_chunk": ms_chunk, "response_ms": ms_chunk,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) bf16 weights, N(0,1) noise/cond)",
+        "config": {"workload": workload_name(cfg_name, cfg), "schedule": "latency (oldest chunk per stream)",
+                   "tasks_per_wave": n_st, "rows_per_wave": n_st * T,
+                   "parallelism": "replicas" if world > 1 else "1 GPU", "graphs": True},
+        "e2e": {"value": world * n_st / (e2e_ms / 1e3), "unit": "chunks/s",
+                "h2d_bytes_per_step": n_st * T * C * 4, "d2h_bytes_per_step": n_st * T * C * 4,
+                "response_ms": e2e_ms},
+        "gpu_launches": (3 + 7 * cfg["B"]) * S * args.steps,
+        "clocks": clk,
+    }
+    sess.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -439,6 +526,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=15.0,
                     help="seconds of CPU time for the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--latency-mode", action="store_true",
+                    help="time the latency-mode schedule (each stream's oldest chunk per wave)")
     ap.add_argument("--blocks", type=int, default=None,
                     help="override the block count (profiling aid: per-block shapes are unchanged)")
     args = ap.parse_args(argv)
@@ -451,6 +540,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, args.config, cfg, world, rank)
+        if args.latency_mode:
+            return run_latency(args, args.config, cfg, world, rank, local)
         return run_psv(args, args.config, cfg, world, rank, local)
     finally:
         if world > 1:

@@ -50,6 +50,11 @@ extern "C" {
                                    step) first: strictly sequential order       */
 #define PSV_FLAG_CHUNK_COND  4  /* reserve per-chunk conditioning tables, for
                                    psv_submit_chunk_cond                       */
+#define PSV_FLAG_LATENCY     8  /* latency mode: a wave runs only each stream's
+                                   oldest ready chunk, so a chunk goes through
+                                   its S steps in S consecutive waves (response
+                                   time S single-chunk waves instead of S full
+                                   waves), at the cost of smaller batches      */
 
 /* ---- model description --------------------------------------------------
  * B blocks, S Euler steps (t_s = 1 - s/S), model width d = H*dh, MLP width

@@ -39,11 +39,23 @@ def ready_tasks(n_stages: int, submitted: list, done: set) -> list:
     return out
 
 
-class WaveSimulator:
-    """Runs waves: every ready task runs; all finish before the next wave."""
+def oldest_per_stream(tasks: list) -> list:
+    """Latency order: of the ready tasks, only each stream's oldest chunk
+    (lowest c) runs, so a chunk goes through its stages back to back."""
+    best = {}
+    for t in tasks:
+        if t[0] not in best or t[1] < best[t[0]][1]:
+            best[t[0]] = t
+    return [t for t in tasks if best[t[0]] is t]
 
-    def __init__(self, n_stages: int):
+
+class WaveSimulator:
+    """Runs waves: every ready task runs (or, with ``latency``, each stream's
+    oldest ready chunk only); all finish before the next wave."""
+
+    def __init__(self, n_stages: int, latency: bool = False):
         self.n_stages = n_stages
+        self.latency = latency
         self.submitted = []
         self.done = set()
 
@@ -56,6 +68,8 @@ class WaveSimulator:
 
     def wave(self) -> list:
         tasks = ready_tasks(self.n_stages, self.submitted, self.done)
+        if self.latency:
+            tasks = oldest_per_stream(tasks)
         self.done.update(tasks)
         return tasks
 

@@ -51,12 +51,12 @@ def _plan_ctx(cfg, max_streams, flags=0, max_inflight=0):
     return P.psv_create(P.model_desc(cfg, max_streams, max_inflight, P.PSV_FLAG_PLAN_ONLY | flags))
 
 
-def _run_schedule(cfg, n_streams, events):
+def _run_schedule(cfg, n_streams, events, latency=False):
     """events: list of ('submit', sid, k) / ('wave',) / ('poll', sid).
     Returns the list of wave plans from the library and the oracle."""
     W = cfg["W"]
-    ctx = _plan_ctx(cfg, n_streams, max_inflight=64)
-    sim = WaveSimulator(cfg["S"])
+    ctx = _plan_ctx(cfg, n_streams, P.PSV_FLAG_LATENCY if latency else 0, max_inflight=64)
+    sim = WaveSimulator(cfg["S"], latency=latency)
     rings = {}
     for _ in range(n_streams):
         assert P.psv_open_stream(ctx, None) == sim.open_stream()
@@ -261,3 +261,28 @@ def test_admission_control_without_measurements():
         P.psv_admit_stream(ctx, None, 0.0)
     assert e.value.code == P.PSV_EAGAIN and "ring" in str(e.value)
     P.psv_destroy(ctx)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_latency_mode_plan_matches_oracle(name):
+    """Latency mode: each stream's oldest ready chunk only, so with all
+    chunks submitted chunk c step s runs in wave c*S + s (its S steps back to
+    back); with staggered submissions the library matches the oracle's
+    brute-force simulator of the same rule."""
+    cfg = synth.config(name)
+    N, S = 5, cfg["S"]
+    lib_w, ora_w = _run_schedule(cfg, 1, [("submit", 0, N)] + [("wave",)] * (N * S + 2), latency=True)
+    assert lib_w == ora_w
+    for w, plan in enumerate(lib_w[: N * S]):
+        assert [(t[1], t[2]) for t in plan] == [(w // S, w % S)]
+    assert lib_w[N * S:] == [[], []]
+    rng = np.random.default_rng(5)
+    events = []
+    for _ in range(40):
+        for sid in range(3):
+            if rng.random() < 0.3:
+                events.append(("submit", sid, int(rng.integers(1, 3))))
+        events.append(("wave",))
+    lib_w, ora_w = _run_schedule(synth.config(name, W=1), 3, events, latency=True)
+    assert lib_w == ora_w
+    assert all(len({t[0] for t in plan}) == len(plan) for plan in lib_w)

@@ -205,9 +205,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_last_p = reinterpret_cast<int*>(tmem_slot + 1);
   float* xch = reinterpret_cast<float*>(tmem_slot + 4);  // [2 key halves][128 rows]
 
+  pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 2 || i == 3) ? 16 : 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  // The peer's barriers must be initialised before anything signals them.
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads what it wrote.
+  pdl_wait();
   // Pair -> (task, head, 256-row query unit, key half), grouped by (task,
   // head) so that the pairs sharing K/V run together while it is in L2.
   const int n_units = (p.T + 2 * QT - 1) / (2 * QT);
@@ -234,20 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qloc0 = unit * 2 * QT + rank * QT;  // first query row of this CTA within the task
   const int item = (ti * p.H + head) * p.max_pairs + unit;
 
-  if (warp == 0 && lane == 0) {
-    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 2 || i == 3) ? 16 : 1);
-    fence_mbar_init();
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  // The peer's barriers must be initialised before anything signals them.
-  cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
@@ -577,17 +581,19 @@ cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUte
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, attn_tc_kernel<DH>, *tmQ, *tmK, *tmV, p);
 }
 

@@ -9,6 +9,23 @@ namespace {
 
 constexpr int LN_WARPS = 8;  // rows per CTA (one warp per row)
 
+// Launch with programmatic stream serialization (see pdl_wait).
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -28,6 +45,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
                   const TaskDev* __restrict__ tasks, const float* __restrict__ table,
                   int use_fmod, int block, int shift_off, int scale_off, float eps) {
   extern __shared__ float4 ln_smem[];  // [2][d / 4]: shift, scale
+  pdl_trigger();
+  pdl_wait();  // h is the previous kernel's output
   const int row0 = blockIdx.x * LN_WARPS;
   const int row = row0 + warp_id();
   const int lane = lane_id();
@@ -105,6 +124,8 @@ __global__ void __launch_bounds__(IP_COLS)
                    int T, const TaskDev* __restrict__ tasks) {
   __shared__ float xs[IP_ROWS][IP_KC + 1];
   __shared__ float ws[IP_KC][IP_COLS + 1];
+  pdl_trigger();
+  pdl_wait();  // the latent state is the previous wave's output
   const int r0 = blockIdx.x * IP_ROWS;
   const int n = blockIdx.y * IP_COLS + threadIdx.x;
   float acc[IP_ROWS];
@@ -216,8 +237,8 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
   const size_t smem = 2 * static_cast<size_t>(nv) * sizeof(float4);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
 #define PSV_LN_LAUNCH(V)                                                                     \
-  ln_mod_kernel<V><<<grid, LN_WARPS * 32, smem, st>>>(h, y, M, d, T, tasks, table,         \
-                                                      use_fmod, block, shift_off, scale_off, eps)
+  return launch_pdl(ln_mod_kernel<V>, dim3(grid), dim3(LN_WARPS * 32), smem, st, h, y, M, d, T, \
+                    tasks, table, use_fmod, block, shift_off, scale_off, eps)
   if (nv <= 32 * 1) PSV_LN_LAUNCH(1);
   else if (nv <= 32 * 2) PSV_LN_LAUNCH(2);
   else if (nv <= 32 * 4) PSV_LN_LAUNCH(4);
@@ -238,8 +259,7 @@ cudaError_t launch_in_proj(const float* state, const __nv_bfloat16* w_in, const 
                            cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   dim3 grid((M + IP_ROWS - 1) / IP_ROWS, (d + IP_COLS - 1) / IP_COLS);
-  in_proj_kernel<<<grid, IP_COLS, 0, st>>>(state, w_in, b_in, h, M, d, C, T, tasks);
-  return cudaGetLastError();
+  return launch_pdl(in_proj_kernel, grid, dim3(IP_COLS), 0, st, state, w_in, b_in, h, M, d, C, T, tasks);
 }
 
 cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat16* W,

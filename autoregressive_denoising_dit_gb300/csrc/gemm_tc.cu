@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* tempty = tfull + 2;                                         // used in the even CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
+  pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
   const int n_m = (p.M + BM - 1) / BM;
   const int n_n = (p.N + BN - 1) / BN;
@@ -286,6 +287,9 @@ __global__ void __launch_bounds__(320, 1)
   // The peer's barriers must be initialised before anything signals them.
   cluster_sync();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads what it wrote.
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -420,11 +424,13 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   static int max_clusters = 0;
   const size_t smem = gemm_smem_bytes();
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(320);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -447,6 +453,7 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   int clusters = max_clusters < n_pt ? max_clusters : n_pt;
   if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
   cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = 2;  // + programmatic stream serialization
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *tmA, *tmB, *tmC, p);
 }
 

@@ -3,15 +3,16 @@
 // A [M, K] bf16 activations and W [N, K] bf16 weights (nn.Linear layout)
 // are both K-major, so TMA loads 128-byte-swizzled tiles that feed
 // tcgen05.mma directly.  CTAs run in pairs (a cluster of two SMs) on 256x256
-// output tiles with 2-SM MMAs (cta_group::2, M = 256): each CTA stages its own
-// 128 rows of A and one 128-row half of the W tile (64 KB per 128-wide k-block,
-// 3 stages), and the even CTA issues every MMA for both.  Per SM this halves
-// the weight traffic and leaves room for a deep TMA pipeline.  Warp roles:
+// output tiles (256x512 for the long-K down-projection, see GemmShape) with
+// 2-SM MMAs (cta_group::2, M = 256): each CTA stages its own 128 rows of A and
+// one 128-row half of the W tile (64 KB per 128-wide k-block, 3 stages), and
+// the even CTA issues every MMA for both.  Per SM this halves the weight
+// traffic and leaves room for a deep TMA pipeline.  Warp roles:
 //   warp 0      TMA producer (both CTAs; completion signalled on the even
 //               CTA's stage barrier)
 //   warp 1      TMEM allocator (both CTAs) + MMA issuer (even CTA only):
 //               256x256x16 MMAs into a double-buffered 2 x 256-column TMEM
-//               accumulator
+//               accumulator (one 512-column accumulator for the wide tile)
 //   warps 2..9  epilogue: tcgen05.ld of this CTA's 128 rows, two warps per
 //               TMEM lane quadrant (128 columns each), the fused epilogue.
 // The tile shape and the K order are fixed for every M, so a row's result
@@ -28,17 +29,36 @@ namespace psv {
 
 namespace {
 
-constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK, STAGES = kGemmStages;
-constexpr int KA = BK / 64;                 // 128-byte swizzle atoms along K per stage
-constexpr int A_ATOM = BM * 128;            // 16 KB: 128 rows x 64 k
-constexpr int B_ATOM = (BN / 2) * 128;      // 16 KB: 128 W rows x 64 k
-constexpr int A_BYTES = KA * A_ATOM;        // this CTA's 128 rows of A
-constexpr int B_BYTES = KA * B_ATOM;        // this CTA's half of the W tile
-static_assert(BK % 64 == 0, "k-block is a whole number of swizzle atoms");
-constexpr uint32_t TMEM_COLS = 512;         // two 256-column accumulators
+constexpr int BM = kGemmBM;
+constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
 constexpr int STAGE_BYTES = 32 * 32 * 4;    // per epilogue warp: a 32 x 32 f32 box
-constexpr uint32_t IDESC = umma_idesc_bf16(2 * BM, BN);  // 256 x 256 per 2-SM MMA
+constexpr uint32_t IDESC = umma_idesc_bf16(2 * BM, 256);  // 256 x 256 per 2-SM MMA
+
+// Pair tile shapes.  Narrow: 256 x 256 per pair, 128-wide k-blocks in 3
+// stages, a double-buffered 2 x 256-column TMEM accumulator (the epilogue of
+// one tile overlaps the MMAs of the next).  Wide: 256 x 512 per pair (two
+// N = 256 MMAs per k-step into all 512 TMEM columns), 64-wide k-blocks in 4
+// stages: a quarter fewer operand bytes per FLOP — the main loop is bound by
+// how fast TMA fills one SM's shared memory — at the price of a single
+// accumulator, so the epilogue is no longer hidden.
+template <bool WIDE>
+struct GemmShape {
+  static constexpr int BN = WIDE ? 512 : 256;   // pair tile width
+  static constexpr int BK = WIDE ? 64 : 128;
+  static constexpr int STAGES = WIDE ? 4 : 3;
+  static constexpr int NSLAB = BN / 256;        // N = 256 MMAs per k-step
+  static constexpr int KA = BK / 64;            // 128-byte swizzle atoms along K per stage
+  static constexpr int A_ATOM = BM * 128;       // 16 KB: 128 rows x 64 k
+  static constexpr int B_ATOM = 128 * 128;      // 16 KB: 128 W rows x 64 k
+  static constexpr int A_BYTES = KA * A_ATOM;   // this CTA's 128 rows of A
+  static constexpr int B_SLAB = KA * B_ATOM;    // this CTA's 128-row half of one N = 256 slab
+  static constexpr int B_BYTES = NSLAB * B_SLAB;
+  static constexpr int ACC_BUFS = WIDE ? 1 : 2;
+  static constexpr size_t SMEM =
+      1024 + STAGES * (A_BYTES + B_BYTES) + EPI_WARPS * STAGE_BYTES + (2 * STAGES + 4) * 8 + 16;
+  static_assert(SMEM <= 232448, "GEMM shared memory over the per-block limit");
+};
 
 // tanh.approx.f32: the SFU's tanh (max relative error ~2^-11, far below the
 // bf16 rounding of the GELU output).
@@ -236,11 +256,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int EPI>
+template <int EPI, bool WIDE>
 __global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using G = GemmShape<WIDE>;
+  constexpr int BN = G::BN, BK = G::BK, STAGES = G::STAGES, KA = G::KA;
+  constexpr int A_ATOM = G::A_ATOM, B_ATOM = G::B_ATOM, A_BYTES = G::A_BYTES, B_BYTES = G::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -311,8 +334,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int a = 0; a < KA; ++a) {
             tma_load_2d_pair(sA + st * A_BYTES + a * A_ATOM, &tmA, bar, kb * BK + a * 64, mb * BM);
-            tma_load_3d_pair(sB + st * B_BYTES + a * B_ATOM, &tmB, bar, kb * BK + a * 64,
-                             nb * BN + rank * (BN / 2), p.wz);
+#pragma unroll
+            for (int sl = 0; sl < G::NSLAB; ++sl)
+              tma_load_3d_pair(sB + st * B_BYTES + sl * G::B_SLAB + a * B_ATOM, &tmB, bar,
+                               kb * BK + a * 64, nb * BN + sl * 256 + rank * 128, p.wz);
           }
         }
       }
@@ -333,11 +358,11 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t a_desc0 = umma_desc_kmajor(smem_u32(sA), 128);
       const uint64_t b_desc0 = umma_desc_kmajor(smem_u32(sB), 128);
       for (int tp = cid; tp < n_pt && ok; tp += n_clusters, ++tc) {
-        const int acc = tc & 1;
-        const uint32_t aph = (tc >> 1) & 1;
+        const int acc = tc % G::ACC_BUFS;
+        const uint32_t aph = (tc / G::ACC_BUFS) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, p.err, ERR_GEMM_TIMEOUT)) break;
         tc_fence_after();
-        const uint32_t dtm = tmem + acc * BN;
+        const uint32_t dtm = tmem + acc * 256;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int st = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -353,7 +378,10 @@ __global__ void __launch_bounds__(320, 1)
             // k-step k: atom k / 4, 32 bytes per step inside the atom
             const uint32_t oa = ((k >> 2) * A_ATOM + (k & 3) * 32) >> 4;
             const uint32_t ob = ((k >> 2) * B_ATOM + (k & 3) * 32) >> 4;
-            umma_bf16_pair(dtm, a + oa, b + ob, IDESC, (kb | k) != 0);
+#pragma unroll
+            for (int sl = 0; sl < G::NSLAB; ++sl)
+              umma_bf16_pair(dtm + sl * 256, a + oa, b + ((sl * G::B_SLAB) >> 4) + ob, IDESC,
+                             (kb | k) != 0);
           }
           umma_commit_pair_mc(&empty[st], 0x3);  // free stage st in both CTAs
         }
@@ -369,12 +397,12 @@ __global__ void __launch_bounds__(320, 1)
     int tc = 0;
     for (int tp = cid; tp < n_pt; tp += n_clusters, ++tc) {
       const int mb = 2 * (tp / n_n) + rank, nb = tp % n_n;
-      const int acc = tc & 1;
-      const uint32_t aph = (tc >> 1) & 1;
+      const int acc = tc % G::ACC_BUFS;
+      const uint32_t aph = (tc / G::ACC_BUFS) & 1;
       if (!warp_wait(&tfull[acc], aph, p.err, ERR_GEMM_TIMEOUT)) break;
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
-      const uint32_t tbase = tmem + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tbase = tmem + acc * 256 + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (EPI == EPI_GELU) {
 #pragma unroll 1
         for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ch += 2) {
@@ -418,11 +446,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, bool WIDE>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                        const GemmParams& p, int max_ctas, cudaStream_t st) {
   static int max_clusters = 0;
-  const size_t smem = gemm_smem_bytes();
+  const size_t smem = GemmShape<WIDE>::SMEM;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -437,42 +465,53 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, WIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(2);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI, WIDE>, &cfg);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_clusters = n;
   }
-  const int n_m = (p.M + BM - 1) / BM, n_n = (p.N + BN - 1) / BN;
+  const int n_m = (p.M + BM - 1) / BM, n_n = (p.N + GemmShape<WIDE>::BN - 1) / GemmShape<WIDE>::BN;
   const int n_pt = ((n_m + 1) / 2) * n_n;
   int clusters = max_clusters < n_pt ? max_clusters : n_pt;
   if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;  // + programmatic stream serialization
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *tmA, *tmB, *tmC, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, WIDE>, *tmA, *tmB, *tmC, p);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() {
-  return 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_WARPS * STAGE_BYTES +
-         (2 * STAGES + 4) * sizeof(uint64_t) + 16;
+  return GemmShape<true>::SMEM > GemmShape<false>::SMEM ? GemmShape<true>::SMEM : GemmShape<false>::SMEM;
 }
+
+// The wide tile pays off only where the main loop is long against the
+// exposed epilogue: the down-projection (K = F).  Measured on the 1.3B wave:
+// down 100 -> 94 us; QKV 66 -> 92, up 105 -> 130, out-projection 29 -> 31 us.
+bool use_wide(int epi, int K) { return epi == EPI_RESID && K >= 4096; }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st) {
   if ((epi == EPI_RESID || epi == EPI_GELU) && !tmC) return cudaErrorInvalidValue;
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
+  const bool wide = use_wide(epi, p.K);
   switch (epi) {
-    case EPI_QKV: return launch_one<EPI_QKV>(tmA, tmB, c, p, grid, st);
-    case EPI_RESID: return launch_one<EPI_RESID>(tmA, tmB, c, p, grid, st);
-    case EPI_GELU: return launch_one<EPI_GELU>(tmA, tmB, c, p, grid, st);
-    case EPI_EULER: return launch_one<EPI_EULER>(tmA, tmB, c, p, grid, st);
+    case EPI_QKV:
+      return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, p, grid, st)
+                  : launch_one<EPI_QKV, false>(tmA, tmB, c, p, grid, st);
+    case EPI_RESID:
+      return wide ? launch_one<EPI_RESID, true>(tmA, tmB, c, p, grid, st)
+                  : launch_one<EPI_RESID, false>(tmA, tmB, c, p, grid, st);
+    case EPI_GELU:
+      return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, p, grid, st)
+                  : launch_one<EPI_GELU, false>(tmA, tmB, c, p, grid, st);
+    case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -74,7 +74,7 @@ size_t attn_counter_ints(int max_tasks, int T, int H);
 // V^T tensor map.
 inline uint32_t attn_v_box_rows(int dh) { return static_cast<uint32_t>(dh / 2); }
 
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 128, kGemmStages = 3;
+constexpr int kGemmBM = 128, kGemmBN = 256;  // rows per CTA, columns of the narrow pair tile
 size_t gemm_smem_bytes();
 size_t attn_smem_bytes(int dh);
 

@@ -62,8 +62,11 @@ struct AttnParams {
 
 // Key tiles (of 256) from which a (task, head, query unit) is split in two
 // halves processed by two CTA pairs; depends on the task's kv_len only, so
-// the result of a task does not depend on the rest of the wave.
-constexpr int kAttnSplitMinTiles = 8;
+// the result of a task does not depend on the rest of the wave.  Splitting
+// doubles the work items and adds a merge through global memory; measured on
+// the 1.3B wave (7800-key windows), not splitting is 12% faster, so only
+// windows of 16K keys and more are split.
+constexpr int kAttnSplitMinTiles = 64;
 // Query units of 256 rows (one CTA pair each) per (task, head).
 int attn_units(int T);
 // CTAs (two per pair) an attention launch over these kv lengths needs.

@@ -20,8 +20,8 @@ def test_noalloc_matches_caller_scratch_on_two_calls():
     import torch
     from autoregressive_denoising_dit_gb300 import _psv as P
 
-    # n=3, T=300, L=2100: split-key path, so partials and counters are used
-    pb = make_problem(n=3, T=300, H=4, dh=64, L=2100, k_rows=2200, vt_cols=2240, seed=7)
+    # L = 16500: split-key path, so partials and counters are used
+    pb = make_problem(n=2, T=300, H=2, dh=64, L=16500, k_rows=16600, vt_cols=16512, seed=7)
     prob = P.AttnProblem(n=pb["n"], T=pb["T"], H=pb["H"], dh=pb["dh"], L=pb["L"],
                          k_rows=pb["k_rows"], vt_cols=pb["vt_cols"])
     assert P.psv_attention_scratch_bytes(prob) <= P.PSV_ATTN_NOALLOC_SCRATCH_BYTES

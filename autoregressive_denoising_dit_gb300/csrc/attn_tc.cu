@@ -71,7 +71,7 @@ struct AttnCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + kStages * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + kStages * V_BYTES;
-  static constexpr int N_BARS = 5 + 4 * kStages;
+  static constexpr int N_BARS = 6 + 4 * kStages;
   // barriers, the TMEM address word, the merge flag, then the row-max /
   // row-sum exchange area [2 key halves][128 rows] f32.  The dynamic
   // shared-memory window starts 1024-byte aligned (no static shared
@@ -195,9 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 0;        // even CTA: both Q tiles landed
   uint64_t* s_full = bars + 1;        // both CTAs: S_j in TMEM
   uint64_t* s_free = bars + 2;        // even CTA: all 16 softmax warps of the pair read S_j
-  uint64_t* p_full = bars + 3;        // even CTA: all 16 softmax warps of the pair wrote P_j
+  uint64_t* p_full_a = bars + 3;      // even CTA: all 16 softmax warps wrote the first half of P_j
   uint64_t* o_done = bars + 4;        // both CTAs: P_j.V_j done (P_j consumed, O stable)
-  uint64_t* k_full = bars + 5;        // [KS] even CTA: both K halves of a stage landed
+  uint64_t* p_full_b = bars + 5;      // even CTA: ... and the second half
+  uint64_t* k_full = bars + 6;        // [KS] even CTA: both K halves of a stage landed
   uint64_t* k_empty = k_full + KS;    // [KS] both CTAs: the S MMA of a stage is done
   uint64_t* v_full = k_empty + KS;    // [VS] even CTA
   uint64_t* v_empty = v_full + VS;    // [VS] both CTAs
@@ -210,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 2 || i == 3) ? 16 : 1);
+    // s_free, p_full_a, p_full_b: every softmax warp of both CTAs arrives
+    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 2 || i == 3 || i == 5) ? 16 : 1);
     fence_mbar_init();
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
@@ -345,17 +347,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!mbar_wait(p_full, j & 1, p.err, ERR_ATTN_TIMEOUT) ||
+        // P_j arrives in two halves: keys [0,64) and [128,192) first (the
+        // first two chunks of each softmax thread), then the rest, so half of
+        // the P.V MMAs issue while the softmax still computes the other half.
+        if (!mbar_wait(p_full_a, j & 1, p.err, ERR_ATTN_TIMEOUT) ||
             !mbar_wait(&v_full[j % VS], (j / VS) & 1, p.err, ERR_ATTN_TIMEOUT))
           break;
         tc_fence_after();
         const uint64_t b = dv + static_cast<uint64_t>(((j % VS) * Cfg::V_BYTES) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
+        auto issue_pv = [&](int kk) {
           // keys [16 kk, 16 kk + 16) of P sit in packed columns [8 kk, 8 kk + 8)
           const uint32_t ov = ((kk >> 2) * Cfg::V_ATOM + (kk & 3) * 32) >> 4;
           umma_pair_tmem_a(tmem + COL_O, tmem + COL_P + kk * 8, b + ov, IDESC_O, (j | kk) != 0);
-        }
+        };
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) issue_pv(kk);
+#pragma unroll
+        for (int kk = 8; kk < 12; ++kk) issue_pv(kk);
+        if (!mbar_wait(p_full_b, j & 1, p.err, ERR_ATTN_TIMEOUT)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 4; kk < 8; ++kk) issue_pv(kk);
+#pragma unroll
+        for (int kk = 12; kk < 16; ++kk) issue_pv(kk);
         umma_commit_pair_mc(o_done, 0x3);
         umma_commit_pair_mc(&v_empty[j % VS], 0x3);
       }
@@ -371,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_addr = tmem + COL_P + hk * 64 + lane_off;
     const uint32_t o_addr = tmem + COL_O + hk * Cfg::OH + lane_off;
     const uint32_t s_free0 = mapa_shared(s_free, 0);
-    const uint32_t p_full0 = mapa_shared(p_full, 0);
+    const uint32_t p_full_a0 = mapa_shared(p_full_a, 0);
+    const uint32_t p_full_b0 = mapa_shared(p_full_b, 0);
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
     bool ok = true;
@@ -444,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) continue;
         tc_fence_after();
       }
-      tmem_st16(p_addr, pk0);
-      tmem_st16(p_addr + 16, pk1);
+      // O is rescaled before the first half of P_j is released: the P_j.V_j
+      // MMAs accumulate into it as soon as that half is in.
       if (j > 0 && any_grow) {
 #pragma unroll 1
         for (int c = 0; c < Cfg::OH / 16; ++c) {
@@ -457,6 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           o_st<16>(o_addr + c * 16, o);
         }
       }
+      tmem_st16(p_addr, pk0);
+      tmem_st16(p_addr + 16, pk1);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(p_full_a0);
       exp_chunk(2, pk0);
       tmem_st16(p_addr + 32, pk0);
       exp_chunk(3, pk1);
@@ -465,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(p_full0);
+      if (lane == 0) mbar_arrive_remote(p_full_b0);
     }
     if (ok) ok = warp_wait(o_done, (nT - 1) & 1, p.err);
     if (ok) tc_fence_after();

@@ -10,8 +10,9 @@
 // invariant to key order).  No mask: a chunk is bidirectional.
 //
 // CTA pairs (clusters of two SMs) with 2-SM tcgen05 MMAs (cta_group::2).  A
-// pair owns 256 query rows of one (task, head), 128 per CTA, and walks the
-// window in tiles of 256 keys.  Per key tile j the even CTA issues
+// work piece is 256 query rows of one (task, head), 128 per CTA, over the
+// whole window or one fixed half of it, walked in tiles of 256 keys.  Per key
+// tile j the even CTA issues
 //   S_j  = Q K_j^T     M=256, N=256, K=dh    (each CTA holds 128 of the keys)
 //   O   += P_j V_j     M=256, N=dh,  K=256   (each CTA holds dh/2 rows of V^T)
 // S, P (bf16, two per TMEM column) and O have TMEM columns of their own, so
@@ -19,7 +20,8 @@
 // it computes the exponentials of tile j.  The wide S MMA (N=256) keeps the one
 // issuing thread well ahead of the tensor pipe.  Warp roles, 384 threads in
 // three warpgroups:
-//   warp 0       TMA: the Q tile, then this CTA's K halves (3 stages)
+//   warp 0       TMA: per piece the Q tile, then this CTA's K halves (3 stages);
+//                on the even CTA also the reader of the work queue
 //   warp 1       TMEM allocator (both CTAs) and MMA issuer (even CTA)
 //   warp 2       TMA: this CTA's V^T halves (3 stages)
 //   warps 4..11  softmax, two threads per query row, 128 keys each of a
@@ -30,11 +32,20 @@
 // (setmaxnreg), so that a softmax thread holds its 128 scores without
 // spilling: local-memory traffic would compete with the MMAs' shared-memory
 // operand reads.
-// Long windows (>= kAttnSplitMinTiles key tiles) are split into two fixed
-// halves handled by two CTA pairs; each half leaves its unnormalised O, m and
-// l in a partial area and the CTA that arrives second on its counter merges
-// both in a fixed order (half 0, half 1), so the result depends neither on
-// which finished first nor on the rest of the wave.
+// Persistent pairs (at most one per two SMs) take pieces from a work queue (a
+// device counter, rewound by the last pair to finish) in a fixed order, large
+// pieces first: the loads, MMAs and softmax run on across piece boundaries
+// (barrier phases and stages count tiles over all of a pair's pieces), so the
+// next piece's Q load and first S MMA overlap the previous piece's last tile
+// and epilogue, and a pair that finishes early takes more work instead of
+// leaving its SMs idle for the rest of the launch.
+// Long windows (>= kAttnSplitMinTiles key tiles) and the short tail units
+// (whose rows fit in the even CTA) are split into two fixed key halves; each
+// half leaves its unnormalised O, m and l in a partial area and the CTA that
+// arrives second on its counter merges both in a fixed order (half 0, half 1).
+// The split depends only on the task's window length and the unit, and the
+// merge order is fixed, so a task's result depends neither on which pair took
+// which piece nor on the rest of the wave.
 #include "psv_device.cuh"
 #include "psv_kernels.h"
 
@@ -52,8 +63,12 @@ constexpr int kStages = 3;                 // K and V^T stages
 // softmax warpgroups grow to kRegsHigh.  The block's launch allocation
 // (threads x registers at launch) must cover the split; the host checks it
 // before the first launch (kRegsNeeded).
-constexpr int kRegsLow = 56, kRegsHigh = 216;
+constexpr int kRegsLow = 64, kRegsHigh = 216;
 constexpr int kRegsNeeded = 128 * kRegsLow + 256 * kRegsHigh;
+// Threads of a pair that take each work piece: the even CTA's MMA issuer, and
+// in both CTAs the V^T loader and one softmax thread; the odd CTA's Q/K loader
+// (the even CTA's one publishes the pieces).
+constexpr int kPieceReaders = 6;
 
 template <int DH>
 struct AttnCfg {
@@ -71,12 +86,13 @@ struct AttnCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + kStages * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + kStages * V_BYTES;
-  static constexpr int N_BARS = 6 + 4 * kStages;
-  // barriers, the TMEM address word, the merge flag, then the row-max /
+  static constexpr int N_BARS = 12 + 4 * kStages;
+  // barriers, the TMEM address word and the merge flag, two published piece
+  // slots and the softmax warps' copy (int4 each), then the row-max /
   // row-sum exchange area [2 key halves][128 rows] f32.  The dynamic
   // shared-memory window starts 1024-byte aligned (no static shared
   // variables; checked at run time).
-  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 2 * QT * 4;
+  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 3 * 16 + 2 * QT * 4;
   static constexpr int OH = DH / 2;              // O columns per thread
   static constexpr int OC = OH < 32 ? OH : 32;   // O columns per TMEM access
   static_assert(V_ATOM % 1024 == 0 && K_ATOM % 1024 == 0, "swizzle atoms stay 1024-aligned");
@@ -168,9 +184,127 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
 }
 
-__host__ __device__ __forceinline__ int n_key_tiles(int kv_len) { return (kv_len + KT - 1) / KT; }
-__host__ __device__ __forceinline__ int n_splits(int kv_len) {
-  return n_key_tiles(kv_len) >= kAttnSplitMinTiles ? 2 : 1;
+// At least one tile per piece (every piece runs the same barrier sequence).
+__host__ __device__ __forceinline__ int n_key_tiles(int kv_len) {
+  return kv_len > KT ? (kv_len + KT - 1) / KT : 1;
+}
+__host__ __device__ __forceinline__ int n_units_of(int T) { return (T + 2 * QT - 1) / (2 * QT); }
+// The last query unit of a task is a tail when all its rows sit in the even
+// CTA (T = 1560: 24 rows).  A tail costs a full unit's MMAs and softmax.
+__host__ __device__ __forceinline__ bool has_tail(int T) {
+  return T - (n_units_of(T) - 1) * 2 * QT <= QT;
+}
+// Key halves of a (task, head, query unit): a function of the task's window
+// and of the unit being a tail only, never of the rest of the launch.  Long
+// windows are split for parallelism; tails are split so that their short
+// halves fill the end of the launch.
+__host__ __device__ __forceinline__ int n_splits(int kv_len, bool tail) {
+  const int nt = n_key_tiles(kv_len);
+  if (nt >= kAttnSplitMinTiles) return 2;
+  if (tail && nt >= kAttnTailSplitMinTiles) return 2;
+  return 1;
+}
+__host__ __device__ __forceinline__ int pieces_main(int kv_len, int T, int H) {
+  return H * (n_units_of(T) - (has_tail(T) ? 1 : 0)) * n_splits(kv_len, false);
+}
+__host__ __device__ __forceinline__ int pieces_tail(int kv_len, int T, int H) {
+  return has_tail(T) ? H * n_splits(kv_len, true) : 0;
+}
+
+// Work piece k of the queue -> {task, head, query unit, half | halves << 8};
+// x = -1 past the end.  Order: the non-tail pieces grouped by (task, head)
+// (the pairs that share a K/V window run together while it is in L2), then
+// the tail pieces, so the shortest pieces fill the end of the launch.
+__device__ int4 decode_piece(int k, const AttnParams& p) {
+  if (k < 0 || k >= p.n_pieces) return make_int4(-1, 0, 0, 0);
+  const int nu = n_units_of(p.T);
+  const bool tail = has_tail(p.T);
+  const int nm = nu - (tail ? 1 : 0);
+  for (int t = 0; t < p.n_tasks; ++t) {
+    const int ns = n_splits(p.tasks[t].kv_len, false);
+    const int c = p.H * nm * ns;
+    if (k < c) return make_int4(t, k / (nm * ns), (k / ns) % nm, (k % ns) | (ns << 8));
+    k -= c;
+  }
+  if (tail) {
+    for (int t = 0; t < p.n_tasks; ++t) {
+      const int ns = n_splits(p.tasks[t].kv_len, true);
+      const int c = p.H * ns;
+      if (k < c) return make_int4(t, k / ns, nu - 1, (k % ns) | (ns << 8));
+      k -= c;
+    }
+  }
+  return make_int4(-1, 0, 0, 0);
+}
+
+struct Piece {
+  int ti, head, unit, half, nsplit;
+  int j_begin, nT;  // key tiles [j_begin, j_begin + nT) of the window
+  int kv_len, row0, ring;
+};
+
+__device__ __forceinline__ Piece piece_of(int4 pc, const AttnParams& p) {
+  Piece g;
+  g.ti = pc.x;
+  g.head = pc.y;
+  g.unit = pc.z;
+  g.half = pc.w & 0xff;
+  g.nsplit = pc.w >> 8;
+  const TaskDev task = p.tasks[g.ti];
+  g.kv_len = task.kv_len;
+  g.row0 = task.row0;
+  g.ring = task.ring0 + p.block * p.S;
+  const int nt = n_key_tiles(g.kv_len);
+  g.j_begin = g.half == 0 ? 0 : nt / 2;
+  g.nT = ((g.nsplit == 1 || g.half == 1) ? nt : nt / 2) - g.j_begin;
+  return g;
+}
+
+// The piece slots are written by the even CTA's thread with st.shared::cluster
+// and published with a release.cluster arrive; readers in either CTA wait
+// with an acquire at cluster scope.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, int4 v) {
+  asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(ptr))
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire (bounded the same way).
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity, int* err,
+                                                      int code) {
+  if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    if ((i & 63) == 63) {
+      if (error_raised(err)) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        raise_error(err, code);
+        return false;
+      }
+    }
+  }
 }
 
 template <int DH>
@@ -192,27 +326,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + Cfg::OFF_K;
   uint8_t* sV = smem + Cfg::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-  uint64_t* q_full = bars + 0;        // even CTA: both Q tiles landed
-  uint64_t* s_full = bars + 1;        // both CTAs: S_j in TMEM
-  uint64_t* s_free = bars + 2;        // even CTA: all 16 softmax warps of the pair read S_j
-  uint64_t* p_full_a = bars + 3;      // even CTA: all 16 softmax warps wrote the first half of P_j
-  uint64_t* o_done = bars + 4;        // both CTAs: P_j.V_j done (P_j consumed, O stable)
+  uint64_t* q_full = bars + 0;        // even CTA: both Q tiles of the current piece landed
+  uint64_t* s_full = bars + 1;        // both CTAs: S of a tile in TMEM
+  uint64_t* s_free = bars + 2;        // even CTA: all 16 softmax warps of the pair read S
+  uint64_t* p_full_a = bars + 3;      // even CTA: all 16 softmax warps wrote the first half of P
+  uint64_t* o_done = bars + 4;        // both CTAs: P.V of a tile done (P consumed, O stable)
   uint64_t* p_full_b = bars + 5;      // even CTA: ... and the second half
-  uint64_t* k_full = bars + 6;        // [KS] even CTA: both K halves of a stage landed
+  uint64_t* q_empty = bars + 6;       // both CTAs: the last S MMA of a piece is done
+  uint64_t* pc_full = bars + 8;       // [2] both CTAs: piece slot published
+  uint64_t* pc_empty = bars + 10;     // [2] even CTA: the pair's six readers took the slot
+  uint64_t* k_full = bars + 12;       // [KS] even CTA: both K halves of a stage landed
   uint64_t* k_empty = k_full + KS;    // [KS] both CTAs: the S MMA of a stage is done
   uint64_t* v_full = k_empty + KS;    // [VS] even CTA
   uint64_t* v_empty = v_full + VS;    // [VS] both CTAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::N_BARS);
   int* s_last_p = reinterpret_cast<int*>(tmem_slot + 1);
-  float* xch = reinterpret_cast<float*>(tmem_slot + 4);  // [2 key halves][128 rows]
+  int4* pc_slot = reinterpret_cast<int4*>(tmem_slot + 4);   // [2] published pieces
+  int4* sm_piece = pc_slot + 2;                             // the softmax warps' copy
+  float* xch = reinterpret_cast<float*>(sm_piece + 1);      // [2 key halves][128 rows]
 
   pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
   if (warp == 0 && lane == 0) {
-    // s_free, p_full_a, p_full_b: every softmax warp of both CTAs arrives
-    for (int i = 0; i < Cfg::N_BARS; ++i) mbar_init(&bars[i], (i == 2 || i == 3 || i == 5) ? 16 : 1);
+    for (int i = 0; i < Cfg::N_BARS; ++i) {
+      // s_free, p_full_a, p_full_b: every softmax warp of both CTAs arrives
+      const bool all16 = i == 2 || i == 3 || i == 5;
+      const bool readers = i == 10 || i == 11;
+      mbar_init(&bars[i], all16 ? 16 : (readers ? kPieceReaders : 1));
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
@@ -226,63 +369,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Everything above overlaps the previous kernel's tail; from here on the
-  // kernel reads what it wrote.
+  // kernel reads what earlier kernels wrote (task table, work queue).
   pdl_wait();
-  // Pair -> (task, head, 256-row query unit, key half), grouped by (task,
-  // head) so that the pairs sharing K/V run together while it is in L2.
-  const int n_units = (p.T + 2 * QT - 1) / (2 * QT);
-  int ti = 0, head = 0, unit = 0, half = 0, nsplit = 1;
-  {
-    int idx = static_cast<int>(blockIdx.x >> 1);
-    for (int t = 0; t < p.n_tasks; ++t) {
-      const int ns = n_splits(p.tasks[t].kv_len);
-      const int cnt = p.H * n_units * ns;
-      if (idx < cnt) {
-        ti = t, nsplit = ns, half = idx % ns, unit = (idx / ns) % n_units, head = idx / (ns * n_units);
-        break;
-      }
-      idx -= cnt;
-    }
-  }
-  const TaskDev task = p.tasks[ti];
-  const int ring = task.ring0 + p.block * p.S;
-  const int kv_len = task.kv_len;
-  const int nT_all = n_key_tiles(kv_len);
-  const int j_begin = (half == 0) ? 0 : nT_all / 2;
-  const int j_end = (nsplit == 1 || half == 1) ? nT_all : nT_all / 2;
-  const int nT = j_end - j_begin;               // key tiles of this pair: [j_begin, j_end)
-  const int qloc0 = unit * 2 * QT + rank * QT;  // first query row of this CTA within the task
-  const int item = (ti * p.H + head) * p.max_pairs + unit;
-
+  const uint32_t pc_empty0 = mapa_shared(pc_empty, 0);
+  // A reader of the pair takes piece i from slot i & 1 and acknowledges it on
+  // the even CTA (after it has used the values, so the slot may be reused).
+  auto take_piece = [&](int i, int4& pc) -> bool {
+    if (!mbar_wait_acq_cluster(&pc_full[i & 1], (i >> 1) & 1, p.err, ERR_ATTN_TIMEOUT)) return false;
+    pc = ld_shared_v4(&pc_slot[i & 1]);
+    mbar_arrive_remote(pc_empty0 + (i & 1) * 8);
+    return true;
+  };
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
       if (lane == 0) {
-        // ---------------- TMA: Q, then K halves; completion counted on the even CTA
+        // ---------------- TMA: per piece the Q tile, then this CTA's K halves
+        // (3 stages, counted over all pieces); completion on the even CTA.
+        // The even CTA's thread also takes the pieces from the work queue and
+        // publishes them to both CTAs.
         const uint32_t q_full0 = mapa_shared(q_full, 0);
         const uint32_t k_full0 = mapa_shared(k_full, 0);
-        if (leader) mbar_arrive_expect_tx(q_full, 2 * Cfg::Q_BYTES);
-#pragma unroll
-        for (int a = 0; a < Cfg::NA; ++a)
-          tma_load_2d_pair(sQ + a * Cfg::Q_ATOM, &tmQ, q_full0, head * DH + a * Cfg::AW,
-                           task.row0 + qloc0);
-        int issued = 0;
-        for (int j = 0; j < nT; ++j) {
-          const int st = j % KS;
-          if (!mbar_wait(&k_empty[st], ((j / KS) & 1) ^ 1, p.err, ERR_ATTN_TIMEOUT)) break;
-          if (leader) mbar_arrive_expect_tx(&k_full[st], 2 * Cfg::K_BYTES);
-          uint8_t* dst = sK + st * Cfg::K_BYTES;
+        int gk = 0;
+        for (int i = 0;; ++i) {
+          int4 pc;
+          if (leader) {
+            const int b = i & 1;
+            if (i >= 2 && !mbar_wait(&pc_empty[b], ((i >> 1) - 1) & 1, p.err, ERR_ATTN_TIMEOUT)) break;
+            pc = decode_piece(atomicAdd(p.counters, 1), p);
+            for (uint32_t r = 0; r < 2; ++r) st_cluster_v4(mapa_shared(&pc_slot[b], r), pc);
+            for (uint32_t r = 0; r < 2; ++r) mbar_arrive_cluster(mapa_shared(&pc_full[b], r));
+          } else if (!take_piece(i, pc)) {
+            break;
+          }
+          if (pc.x < 0) break;
+          const Piece pg = piece_of(pc, p);
+          // The Q buffer is reused once the previous piece's S MMAs are done.
+          if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, p.err, ERR_ATTN_TIMEOUT)) break;
+          if (leader) mbar_arrive_expect_tx(q_full, 2 * Cfg::Q_BYTES);
 #pragma unroll
           for (int a = 0; a < Cfg::NA; ++a)
-            tma_load_3d_pair(dst + a * Cfg::K_ATOM, &tmK, k_full0 + st * 8, head * DH + a * Cfg::AW,
-                             (j_begin + j) * KT + rank * 128, ring);
-          ++issued;
+            tma_load_2d_pair(sQ + a * Cfg::Q_ATOM, &tmQ, q_full0, pg.head * DH + a * Cfg::AW,
+                             pg.row0 + pg.unit * 2 * QT + rank * QT);
+          bool ok = true;
+          for (int j = 0; j < pg.nT; ++j, ++gk) {
+            const int st = gk % KS;
+            if (!mbar_wait(&k_empty[st], ((gk / KS) & 1) ^ 1, p.err, ERR_ATTN_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(&k_full[st], 2 * Cfg::K_BYTES);
+            uint8_t* dst = sK + st * Cfg::K_BYTES;
+#pragma unroll
+            for (int a = 0; a < Cfg::NA; ++a)
+              tma_load_3d_pair(dst + a * Cfg::K_ATOM, &tmK, k_full0 + st * 8, pg.head * DH + a * Cfg::AW,
+                               (pg.j_begin + j) * KT + rank * 128, pg.ring);
+          }
+          if (!ok) break;
         }
         // Stay until the MMAs released the last stages (bounded): no copy into
         // or read of this CTA's shared memory may be left when it exits.
         const uint64_t t0 = global_timer_ns();
-        for (int j = (issued > KS ? issued - KS : 0); j < issued; ++j) {
+        for (int j = (gk > KS ? gk - KS : 0); j < gk; ++j) {
           while (!mbar_try_wait(&k_empty[j % KS], (j / KS) & 1) &&
                  global_timer_ns() - t0 < kWaitLimitNs) {
           }
@@ -292,37 +441,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ---------------- TMA: V^T halves (dh/2 rows of this CTA, 256 keys)
         const uint32_t v_full0 = mapa_shared(v_full, 0);
-        int issued = 0;
-        for (int j = 0; j < nT; ++j) {
-          const int st = j % VS;
-          if (!mbar_wait(&v_empty[st], ((j / VS) & 1) ^ 1, p.err, ERR_ATTN_TIMEOUT)) break;
-          if (leader) mbar_arrive_expect_tx(&v_full[st], 2 * Cfg::V_BYTES);
-          uint8_t* dst = sV + st * Cfg::V_BYTES;
+        int gv = 0;
+        for (int i = 0;; ++i) {
+          int4 pc;
+          if (!take_piece(i, pc) || pc.x < 0) break;
+          const Piece pg = piece_of(pc, p);
+          bool ok = true;
+          for (int j = 0; j < pg.nT; ++j, ++gv) {
+            const int st = gv % VS;
+            if (!mbar_wait(&v_empty[st], ((gv / VS) & 1) ^ 1, p.err, ERR_ATTN_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(&v_full[st], 2 * Cfg::V_BYTES);
+            uint8_t* dst = sV + st * Cfg::V_BYTES;
 #pragma unroll
-          for (int a = 0; a < KT / 64; ++a)
-            tma_load_3d_pair(dst + a * Cfg::V_ATOM, &tmV, v_full0 + st * 8,
-                             (j_begin + j) * KT + a * 64, rank * Cfg::VR, ring * p.H + head);
-          ++issued;
+            for (int a = 0; a < KT / 64; ++a)
+              tma_load_3d_pair(dst + a * Cfg::V_ATOM, &tmV, v_full0 + st * 8,
+                               (pg.j_begin + j) * KT + a * 64, rank * Cfg::VR, pg.ring * p.H + pg.head);
+          }
+          if (!ok) break;
         }
         const uint64_t t0 = global_timer_ns();
-        for (int j = (issued > VS ? issued - VS : 0); j < issued; ++j) {
+        for (int j = (gv > VS ? gv - VS : 0); j < gv; ++j) {
           while (!mbar_try_wait(&v_empty[j % VS], (j / VS) & 1) &&
                  global_timer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
     } else if (warp == 1 && lane == 0 && leader) {
-      // ---------------- MMA issuer (even CTA), 2-SM MMAs for the pair, in
-      // this order: S_0, then per tile j: S_{j+1} once every softmax warp has
-      // read S_j (and K_{j+1} is in), P_j.V_j once every softmax warp has
-      // written P_j (and V_j is in).  Issue order is execution order.
+      // ---------------- MMA issuer (even CTA), 2-SM MMAs for the pair.  Per
+      // piece: S_0 once its Q is in (and the softmax read the previous tile's
+      // S), then per tile j: S_{j+1} once every softmax warp has read S_j (and
+      // K_{j+1} is in), P_j.V_j once every softmax warp has written P_j (and
+      // V_j is in).  Issue order is execution order; tiles are counted over
+      // all pieces of the pair (barrier phases, K/V stages).
       constexpr uint32_t IDESC_S = umma_idesc_bf16(2 * QT, KT);
       constexpr uint32_t IDESC_O = umma_idesc_bf16(2 * QT, DH);
       const uint64_t dq = umma_desc_kmajor(smem_u32(sQ), Cfg::ROWB);
       const uint64_t dk = umma_desc_kmajor(smem_u32(sK), Cfg::ROWB);
       const uint64_t dv = umma_desc_kmajor(smem_u32(sV), 128);
-      auto issue_s = [&](int i) {
-        const uint64_t b = dk + static_cast<uint64_t>(((i % KS) * Cfg::K_BYTES) >> 4);
+      auto issue_s = [&](int t) {
+        const uint64_t b = dk + static_cast<uint64_t>(((t % KS) * Cfg::K_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const int e = kk * 16;
@@ -331,47 +491,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_pair(tmem + COL_S, dq + oq, b + ok, IDESC_S, kk != 0);
         }
         umma_commit_pair_mc(s_full, 0x3);
-        umma_commit_pair_mc(&k_empty[i % KS], 0x3);
+        umma_commit_pair_mc(&k_empty[t % KS], 0x3);
       };
-      bool ok = mbar_wait(q_full, 0, p.err, ERR_ATTN_TIMEOUT) &&
-                mbar_wait(&k_full[0], 0, p.err, ERR_ATTN_TIMEOUT);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 0; j < nT && ok; ++j) {
-        if (j + 1 < nT) {
-          if (!mbar_wait(s_free, j & 1, p.err, ERR_ATTN_TIMEOUT) ||
-              !mbar_wait(&k_full[(j + 1) % KS], ((j + 1) / KS) & 1, p.err, ERR_ATTN_TIMEOUT))
-            break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        // P_j arrives in two halves: keys [0,64) and [128,192) first (the
-        // first two chunks of each softmax thread), then the rest, so half of
-        // the P.V MMAs issue while the softmax still computes the other half.
-        if (!mbar_wait(p_full_a, j & 1, p.err, ERR_ATTN_TIMEOUT) ||
-            !mbar_wait(&v_full[j % VS], (j / VS) & 1, p.err, ERR_ATTN_TIMEOUT))
+      int g = 0;  // tiles of earlier pieces
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        int4 pc;
+        if (!take_piece(i, pc) || pc.x < 0) break;
+        const int nT = piece_of(pc, p).nT;
+        if (!mbar_wait(q_full, i & 1, p.err, ERR_ATTN_TIMEOUT) ||
+            !mbar_wait(&k_full[g % KS], (g / KS) & 1, p.err, ERR_ATTN_TIMEOUT) ||
+            (g > 0 && !mbar_wait(s_free, (g - 1) & 1, p.err, ERR_ATTN_TIMEOUT)))
           break;
         tc_fence_after();
-        const uint64_t b = dv + static_cast<uint64_t>(((j % VS) * Cfg::V_BYTES) >> 4);
-        auto issue_pv = [&](int kk) {
-          // keys [16 kk, 16 kk + 16) of P sit in packed columns [8 kk, 8 kk + 8)
-          const uint32_t ov = ((kk >> 2) * Cfg::V_ATOM + (kk & 3) * 32) >> 4;
-          umma_pair_tmem_a(tmem + COL_O, tmem + COL_P + kk * 8, b + ov, IDESC_O, (j | kk) != 0);
-        };
+        issue_s(g);
+        // After the piece's last S MMA the Q buffer may be refilled once it is done.
+        if (nT == 1) umma_commit_pair_mc(q_empty, 0x3);
+        for (int j = 0; j < nT; ++j) {
+          const int t = g + j;
+          if (j + 1 < nT) {
+            if (!mbar_wait(s_free, t & 1, p.err, ERR_ATTN_TIMEOUT) ||
+                !mbar_wait(&k_full[(t + 1) % KS], ((t + 1) / KS) & 1, p.err, ERR_ATTN_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t + 1);
+            if (j + 2 == nT) umma_commit_pair_mc(q_empty, 0x3);
+          }
+          // P_j arrives in two halves: keys [0,64) and [128,192) first (the
+          // first two chunks of each softmax thread), then the rest, so half
+          // of the P.V MMAs issue while the softmax still computes the other
+          // half.  A piece's first P.V overwrites O: the softmax warps read
+          // the previous piece's O before they wrote any of this P.
+          if (!mbar_wait(p_full_a, t & 1, p.err, ERR_ATTN_TIMEOUT) ||
+              !mbar_wait(&v_full[t % VS], (t / VS) & 1, p.err, ERR_ATTN_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t b = dv + static_cast<uint64_t>(((t % VS) * Cfg::V_BYTES) >> 4);
+          auto issue_pv = [&](int kk) {
+            // keys [16 kk, 16 kk + 16) of P sit in packed columns [8 kk, 8 kk + 8)
+            const uint32_t ov = ((kk >> 2) * Cfg::V_ATOM + (kk & 3) * 32) >> 4;
+            umma_pair_tmem_a(tmem + COL_O, tmem + COL_P + kk * 8, b + ov, IDESC_O, (j | kk) != 0);
+          };
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) issue_pv(kk);
+          for (int kk = 0; kk < 4; ++kk) issue_pv(kk);
 #pragma unroll
-        for (int kk = 8; kk < 12; ++kk) issue_pv(kk);
-        if (!mbar_wait(p_full_b, j & 1, p.err, ERR_ATTN_TIMEOUT)) break;
-        tc_fence_after();
+          for (int kk = 8; kk < 12; ++kk) issue_pv(kk);
+          if (!mbar_wait(p_full_b, t & 1, p.err, ERR_ATTN_TIMEOUT)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 4; kk < 8; ++kk) issue_pv(kk);
+          for (int kk = 4; kk < 8; ++kk) issue_pv(kk);
 #pragma unroll
-        for (int kk = 12; kk < 16; ++kk) issue_pv(kk);
-        umma_commit_pair_mc(o_done, 0x3);
-        umma_commit_pair_mc(&v_empty[j % VS], 0x3);
+          for (int kk = 12; kk < 16; ++kk) issue_pv(kk);
+          umma_commit_pair_mc(o_done, 0x3);
+          umma_commit_pair_mc(&v_empty[t % VS], 0x3);
+        }
+        g += nT;
       }
     }
   } else {
@@ -388,185 +569,209 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_full_a0 = mapa_shared(p_full_a, 0);
     const uint32_t p_full_b0 = mapa_shared(p_full_b, 0);
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
-    bool ok = true;
-    // Every softmax warp runs all nT iterations and every named barrier, also
-    // after a failed wait (which only skips the work), so barrier counts match.
-    for (int j = 0; j < nT; ++j) {
-      if (ok) ok = warp_wait(s_full, j & 1, p.err);
-      float s[128];
-      float mx_half = -INFINITY;
-      const int key0 = (j_begin + j) * KT + hk * 128;
-      if (ok) {
-        tc_fence_after();
+    int g = 0;  // tiles of earlier pieces
+    for (int i = 0;; ++i) {
+      // One thread takes the piece for the CTA's eight softmax warps, so that
+      // all of them run the same pieces and named barriers (also after an
+      // error, which ends the loop for all).  The copy is rewritten only after
+      // every warp has passed this piece's later barriers.
+      if (warp == 4 && lane == 0) {
+        int4 pc;
+        if (!take_piece(i, pc)) pc.x = -1;
+        *sm_piece = pc;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const int4 pc = ld_shared_v4(sm_piece);
+      if (pc.x < 0) break;
+      const Piece pg = piece_of(pc, p);
+      const int nT = pg.nT;
+      float m = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
+      bool ok = true;
+      // Every softmax warp runs all nT iterations and every named barrier, also
+      // after a failed wait (which only skips the work), so barrier counts match.
+      for (int j = 0; j < nT; ++j) {
+        const int t = g + j;
+        if (ok) ok = warp_wait(s_full, t & 1, p.err);
+        float s[128];
+        float mx_half = -INFINITY;
+        const int key0 = (pg.j_begin + j) * KT + hk * 128;
+        if (ok) {
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, s + c * 32);
-        tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, s + c * 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(s_free0);  // S may now be overwritten
+          if (key0 + 128 > pg.kv_len) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (key0 + c >= pg.kv_len) s[c] = -INFINITY;
+          }
+          float mx8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = max3(s[e], s[e + 8], s[e + 16]);
+#pragma unroll
+          for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = max3(mx8[e], s[c + e], s[c + 8 + e]);
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[120 + e]);
+          mx_half = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
+                          fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        }
+        // Row max over both key halves (shared-memory exchange).
+        xch[hk * QT + r] = mx_half;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float other_mx = xch[(1 - hk) * QT + r];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (!ok) continue;
+        const float m_tile = fmaxf(mx_half, other_mx) * sl2;
+        const bool grow = m_tile > m + kRescaleThreshold;
+        const bool any_grow = __any_sync(0xffffffffu, grow);
+        const float m_new = grow ? m_tile : m;
+        const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
+        // P = exp2(s * scale_log2 - m) in bf16, 32 keys (16 packed columns) per
+        // chunk.  The first two chunks are computed before waiting for the
+        // previous tile's P to be consumed, the rest after it.
+        const float negm = -m_new;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        auto exp_chunk = [&](int c, uint32_t* pk) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a = s[c * 32 + 2 * e], b = s[c * 32 + 2 * e + 1];
+            ffma2(a, b, sl2, negm);
+            a = fast_exp2(a);
+            b = fast_exp2(b);
+            fadd2(acc[2 * (e & 3)], acc[2 * (e & 3) + 1], a, b);
+            pk[e] = pack_bf16x2(a, b);
+          }
+        };
+        uint32_t pk0[16], pk1[16];
+        exp_chunk(0, pk0);
+        exp_chunk(1, pk1);
+        m = m_new;
+        if (j > 0) {
+          ok = warp_wait(o_done, (t - 1) & 1, p.err);
+          if (!ok) continue;
+          tc_fence_after();
+        }
+        // O is rescaled before the first half of P is released: the P.V MMAs
+        // accumulate into it as soon as that half is in.
+        if (j > 0 && any_grow) {
+#pragma unroll 1
+          for (int c = 0; c < Cfg::OH / 16; ++c) {
+            float o[16];
+            tmem_ld16f(o_addr + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            o_st<16>(o_addr + c * 16, o);
+          }
+        }
+        tmem_st16(p_addr, pk0);
+        tmem_st16(p_addr + 16, pk1);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(s_free0);  // S_j may now be overwritten
-        if (key0 + 128 > kv_len) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (key0 + c >= kv_len) s[c] = -INFINITY;
-        }
-        float mx8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = max3(s[e], s[e + 8], s[e + 16]);
-#pragma unroll
-        for (int c = 24; c < 120; c += 16) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = max3(mx8[e], s[c + e], s[c + 8 + e]);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[120 + e]);
-        mx_half = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
-                        fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        if (lane == 0) mbar_arrive_remote(p_full_a0);
+        exp_chunk(2, pk0);
+        tmem_st16(p_addr + 32, pk0);
+        exp_chunk(3, pk1);
+        tmem_st16(p_addr + 48, pk1);
+        l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(p_full_b0);
       }
-      // Row max over both key halves (shared-memory exchange).
-      xch[hk * QT + r] = mx_half;
+      if (ok) ok = warp_wait(o_done, (g + nT - 1) & 1, p.err);
+      if (ok) tc_fence_after();
+      g += nT;
+      // Row sum over both key halves, fixed order (half 0 + half 1).
+      xch[hk * QT + r] = l;
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      const float other_mx = xch[(1 - hk) * QT + r];
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (!ok) continue;
-      const float m_tile = fmaxf(mx_half, other_mx) * sl2;
-      const bool grow = m_tile > m + kRescaleThreshold;
-      const bool any_grow = __any_sync(0xffffffffu, grow);
-      const float m_new = grow ? m_tile : m;
-      const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
-      // P = exp2(s * scale_log2 - m) in bf16, 32 keys (16 packed columns) per
-      // chunk.  The first two chunks are computed before waiting for P_{j-1}
-      // to be consumed, the rest after it.
-      const float negm = -m_new;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      auto exp_chunk = [&](int c, uint32_t* pk) {
+      l = xch[r] + xch[QT + r];
+      // O is read (below) before this thread writes any P of the next piece,
+      // whose first P.V overwrites it.
+      const int qloc0 = pg.unit * 2 * QT + rank * QT;  // first query row of this CTA within the task
+      const int item = (pg.ti * p.H + pg.head) * p.max_pairs + pg.unit;
+      const bool valid = (qloc0 + r) < p.T;
+      __nv_bfloat16* dst = p.o + static_cast<int64_t>(pg.row0 + qloc0 + r) * p.d + pg.head * DH +
+                           hk * Cfg::OH;
+      auto store_row = [&](const float* v, int c, float inv) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * Cfg::OC);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float a = s[c * 32 + 2 * e], b = s[c * 32 + 2 * e + 1];
-          ffma2(a, b, sl2, negm);
-          a = fast_exp2(a);
-          b = fast_exp2(b);
-          fadd2(acc[2 * (e & 3)], acc[2 * (e & 3) + 1], a, b);
-          pk[e] = pack_bf16x2(a, b);
+        for (int e = 0; e < Cfg::OC / 8; ++e) {
+          uint4 w;
+          w.x = pack_bf16x2(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
+          w.y = pack_bf16x2(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
+          w.z = pack_bf16x2(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
+          w.w = pack_bf16x2(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
+          d4[e] = w;
         }
       };
-      uint32_t pk0[16], pk1[16];
-      exp_chunk(0, pk0);
-      exp_chunk(1, pk1);
-      m = m_new;
-      if (j > 0) {
-        ok = warp_wait(o_done, (j - 1) & 1, p.err);
-        if (!ok) continue;
-        tc_fence_after();
-      }
-      // O is rescaled before the first half of P_j is released: the P_j.V_j
-      // MMAs accumulate into it as soon as that half is in.
-      if (j > 0 && any_grow) {
+      if (pg.nsplit == 1) {
+        if (ok) {
+          const float inv_l = 1.0f / l;
 #pragma unroll 1
-        for (int c = 0; c < Cfg::OH / 16; ++c) {
-          float o[16];
-          tmem_ld16f(o_addr + c * 16, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          o_st<16>(o_addr + c * 16, o);
-        }
-      }
-      tmem_st16(p_addr, pk0);
-      tmem_st16(p_addr + 16, pk1);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(p_full_a0);
-      exp_chunk(2, pk0);
-      tmem_st16(p_addr + 32, pk0);
-      exp_chunk(3, pk1);
-      tmem_st16(p_addr + 48, pk1);
-      l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(p_full_b0);
-    }
-    if (ok) ok = warp_wait(o_done, (nT - 1) & 1, p.err);
-    if (ok) tc_fence_after();
-    // Row sum over both key halves, fixed order (half 0 + half 1).
-    xch[hk * QT + r] = l;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    l = xch[r] + xch[QT + r];
-    const bool valid = (qloc0 + r) < p.T;
-    __nv_bfloat16* dst =
-        p.o + static_cast<int64_t>(task.row0 + qloc0 + r) * p.d + head * DH + hk * Cfg::OH;
-    auto store_row = [&](const float* o, int c, float inv) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * Cfg::OC);
-#pragma unroll
-      for (int e = 0; e < Cfg::OC / 8; ++e) {
-        uint4 w;
-        w.x = pack_bf16x2(o[8 * e + 0] * inv, o[8 * e + 1] * inv);
-        w.y = pack_bf16x2(o[8 * e + 2] * inv, o[8 * e + 3] * inv);
-        w.z = pack_bf16x2(o[8 * e + 4] * inv, o[8 * e + 5] * inv);
-        w.w = pack_bf16x2(o[8 * e + 6] * inv, o[8 * e + 7] * inv);
-        d4[e] = w;
-      }
-    };
-    if (nsplit == 1) {
-      if (ok) {
-        const float inv_l = 1.0f / l;
-#pragma unroll 1
-        for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
-          float o[Cfg::OC];
-          o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
-          tmem_wait_ld();
-          if (valid) store_row(o, c, inv_l);
-        }
-      }
-    } else {
-      // Leave this key half's unnormalised O, m, l; the CTA with the same
-      // query rows in the other key half's pair that arrives second merges.
-      constexpr int PART = (DH + 2) * QT;
-      float* base = p.part + static_cast<int64_t>(item) * 4 * PART;
-      float* mine = base + (half * 2 + rank) * PART;
-      const float* other = base + ((1 - half) * 2 + rank) * PART;
-      int* counter = p.counters + item * 2 + rank;
-      if (ok) {
-#pragma unroll 1
-        for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
-          float o[Cfg::OC];
-          o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < Cfg::OC; ++e) mine[(hk * Cfg::OH + c * Cfg::OC + e) * QT + r] = o[e];
-        }
-        if (hk == 0) {
-          mine[DH * QT + r] = m;
-          mine[(DH + 1) * QT + r] = l;
-        }
-      }
-      __threadfence();
-      asm volatile("bar.sync 2, 256;" ::: "memory");
-      if (warp == 4 && lane == 0)
-        *s_last_p = (ok && !error_raised(p.err)) ? atomicAdd(counter, 1) : -1;
-      asm volatile("bar.sync 2, 256;" ::: "memory");
-      if (*s_last_p == 1) {
-        __threadfence();
-        const float* h0 = half == 0 ? mine : other;
-        const float* h1 = half == 0 ? other : mine;
-        const float m0 = __ldcg(h0 + DH * QT + r), m1 = __ldcg(h1 + DH * QT + r);
-        const float l0 = __ldcg(h0 + (DH + 1) * QT + r), l1 = __ldcg(h1 + (DH + 1) * QT + r);
-        const float mm = fmaxf(m0, m1);
-        const float a0 = fast_exp2(m0 - mm), a1 = fast_exp2(m1 - mm);
-        const float inv = 1.0f / (l0 * a0 + l1 * a1);
-#pragma unroll 1
-        for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
-          float o[Cfg::OC];
-#pragma unroll
-          for (int e = 0; e < Cfg::OC; ++e) {
-            const int k = (hk * Cfg::OH + c * Cfg::OC + e) * QT + r;
-            o[e] = __ldcg(h0 + k) * a0 + __ldcg(h1 + k) * a1;
+          for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
+            float o[Cfg::OC];
+            o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
+            tmem_wait_ld();
+            if (valid) store_row(o, c, inv_l);
           }
-          if (valid) store_row(o, c, inv);
         }
-        if (warp == 4 && lane == 0) *counter = 0;
+      } else {
+        // Leave this key half's unnormalised O, m, l; the CTA with the same
+        // query rows in the other key half's pair that arrives second merges.
+        constexpr int PART = (DH + 2) * QT;
+        float* base = p.part + static_cast<int64_t>(item) * 4 * PART;
+        float* mine = base + (pg.half * 2 + rank) * PART;
+        const float* other = base + ((1 - pg.half) * 2 + rank) * PART;
+        int* counter = p.counters + kQueueInts + item * 2 + rank;
+        if (ok) {
+#pragma unroll 1
+          for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
+            float o[Cfg::OC];
+            o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < Cfg::OC; ++e) mine[(hk * Cfg::OH + c * Cfg::OC + e) * QT + r] = o[e];
+          }
+          if (hk == 0) {
+            mine[DH * QT + r] = m;
+            mine[(DH + 1) * QT + r] = l;
+          }
+        }
+        __threadfence();
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (warp == 4 && lane == 0)
+          *s_last_p = (ok && !error_raised(p.err)) ? atomicAdd(counter, 1) : -1;
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (*s_last_p == 1) {
+          __threadfence();
+          const float* h0 = pg.half == 0 ? mine : other;
+          const float* h1 = pg.half == 0 ? other : mine;
+          const float m0 = __ldcg(h0 + DH * QT + r), m1 = __ldcg(h1 + DH * QT + r);
+          const float l0 = __ldcg(h0 + (DH + 1) * QT + r), l1 = __ldcg(h1 + (DH + 1) * QT + r);
+          const float mm = fmaxf(m0, m1);
+          const float a0 = fast_exp2(m0 - mm), a1 = fast_exp2(m1 - mm);
+          const float inv = 1.0f / (l0 * a0 + l1 * a1);
+#pragma unroll 1
+          for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
+            float o[Cfg::OC];
+#pragma unroll
+            for (int e = 0; e < Cfg::OC; ++e) {
+              const int k = (hk * Cfg::OH + c * Cfg::OC + e) * QT + r;
+              o[e] = __ldcg(h0 + k) * a0 + __ldcg(h1 + k) * a1;
+            }
+            if (valid) store_row(o, c, inv);
+          }
+          if (warp == 4 && lane == 0) *counter = 0;
+        }
+        // s_last_p is rewritten only after the next piece's first barrier.
       }
     }
   }
@@ -580,6 +785,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+  if (leader && warp == 0 && lane == 0) {
+    // The last pair to finish rewinds the work queue for the next launch
+    // (every pair took its final, empty piece before counting itself done).
+    __threadfence();
+    if (atomicAdd(p.counters + 1, 1) == static_cast<int>(gridDim.x / 2) - 1) {
+      atomicExch(p.counters, 0);
+      atomicExch(p.counters + 1, 0);
+    }
   }
 }
 
@@ -669,10 +883,15 @@ cudaError_t launch_fill_attn_tasks(TaskDev* tasks, int n, int T, int L, cudaStre
 
 int attn_units(int T) { return (T + 2 * QT - 1) / (2 * QT); }
 
-int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H) {
+int attn_pieces(const int* kv_lens, int n_tasks, int T, int H) {
   int total = 0;
-  for (int t = 0; t < n_tasks; ++t) total += 2 * H * attn_units(T) * n_splits(kv_lens[t]);
+  for (int t = 0; t < n_tasks; ++t) total += pieces_main(kv_lens[t], T, H) + pieces_tail(kv_lens[t], T, H);
   return total;
+}
+
+int attn_grid_size(int n_pieces, int sm_count) {
+  const int pairs_max = sm_count / 2 > 0 ? sm_count / 2 : 1;
+  return 2 * (n_pieces < pairs_max ? n_pieces : pairs_max);
 }
 
 size_t attn_part_floats(int max_tasks, int T, int H, int dh) {
@@ -680,7 +899,7 @@ size_t attn_part_floats(int max_tasks, int T, int H, int dh) {
 }
 
 size_t attn_counter_ints(int max_tasks, int T, int H) {
-  return static_cast<size_t>(max_tasks) * H * attn_units(T) * 2;
+  return kQueueInts + static_cast<size_t>(max_tasks) * H * attn_units(T) * 2;
 }
 
 }  // namespace psv

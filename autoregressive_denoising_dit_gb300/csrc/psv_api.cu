@@ -494,7 +494,8 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     attn_bytes += (2.0 * m.T * d + 2.0 * static_cast<double>(t.kv_len) * d) * 2.0;
     kv_lens.push_back(t.kv_len);
   }
-  const int attn_grid = psv::attn_grid_size(kv_lens.data(), n, m.T, m.H);
+  const int attn_pieces = psv::attn_pieces(kv_lens.data(), n, m.T, m.H);
+  const int attn_grid = psv::attn_grid_size(attn_pieces, ctx->sm_count);
 
   for (int b = 0; b < m.B; ++b) {
     if (tap && b == ctx->tap_block && run.err == cudaSuccess)
@@ -539,6 +540,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       a.part = ctx->at<float>(L.attn_part);
       a.counters = ctx->at<int>(L.attn_cnt);
       a.max_pairs = L.attn_pairs;
+      a.n_pieces = attn_pieces;
       a.err = ctx->at<int>(L.err);
       run.run(K_ATTN, attn_flops, attn_bytes, [&] {
         return psv::launch_attention(&ctx->tmQ, &ctx->tmK, &ctx->tmV, a, n, attn_grid, st);
@@ -1186,11 +1188,11 @@ PSV_API int psv_run_wave(psv_ctx* ctx, int* n_tasks) {
       ctx->tap_block = -1;
     } else {
       // A wave's launches depend on its task count and on how many attention
-      // CTAs its windows need (fill waves have shorter windows).
+      // work pieces its windows make (fill waves have shorter windows).
       std::vector<int> kvl;
       for (const TaskDev& t : dev) kvl.push_back(t.kv_len);
       const int64_t key = (static_cast<int64_t>(n) << 32) |
-                          static_cast<int64_t>(psv::attn_grid_size(kvl.data(), n, ctx->m.T, ctx->m.H));
+                          static_cast<int64_t>(psv::attn_pieces(kvl.data(), n, ctx->m.T, ctx->m.H));
       int& seen = ctx->shape_seen[key];
       auto it = ctx->graphs.find(key);
       if (it == ctx->graphs.end() && seen >= 1) {

@@ -52,11 +52,13 @@ struct AttnParams {
   __nv_bfloat16* o;        // [rows][d]
   float scale_log2;        // log2(e) / sqrt(dh)
   // Split-KV partials: per (task, head, 256-row query unit) 2 key halves x
-  // 2 CTAs of [dh + 2][128] f32 (O transposed, then m, l), and one arrival
-  // counter per (unit, CTA).
+  // 2 CTAs of [dh + 2][128] f32 (O transposed, then m, l).  counters: the
+  // work queue (kQueueInts: next piece, pairs done; zero between launches),
+  // then one arrival counter per (unit, CTA).
   float* part;
   int* counters;
   int max_pairs;           // query units per (task, head) the partial area is sized for
+  int n_pieces;            // work pieces of this launch (attn_pieces)
   int* err;
 };
 
@@ -67,10 +69,19 @@ struct AttnParams {
 // the 1.3B wave (7800-key windows), not splitting is 12% faster, so only
 // windows of 16K keys and more are split.
 constexpr int kAttnSplitMinTiles = 64;
-// Query units of 256 rows (one CTA pair each) per (task, head).
+// Tail units (the last query unit of a task when its rows fit in one CTA,
+// e.g. 24 of T = 1560) cost as much as a full unit; from this many key tiles
+// they are split into two halves, which the work queue hands out last so that
+// they fill the end of the launch.
+constexpr int kAttnTailSplitMinTiles = 8;
+constexpr int kQueueInts = 2;
+// Query units of 256 rows per (task, head).
 int attn_units(int T);
-// CTAs (two per pair) an attention launch over these kv lengths needs.
-int attn_grid_size(const int* kv_lens, int n_tasks, int T, int H);
+// Work pieces (256 query rows x a whole window or one key half) of a launch
+// over these kv lengths.
+int attn_pieces(const int* kv_lens, int n_tasks, int T, int H);
+// CTAs (two per pair) of a persistent launch: one pair per two SMs at most.
+int attn_grid_size(int n_pieces, int sm_count);
 size_t attn_part_floats(int max_tasks, int T, int H, int dh);
 size_t attn_counter_ints(int max_tasks, int T, int H);
 // Each CTA of a pair loads dh/2 rows of a V^T tile: the box height of the

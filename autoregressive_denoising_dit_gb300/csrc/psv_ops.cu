@@ -110,7 +110,12 @@ int psv_attention_enqueue(const psv_attn_problem* p, const void* q, const void* 
   a.max_pairs = psv::attn_units(p->T);
   a.err = reinterpret_cast<int*>(scratch + L.err);
   std::vector<int> kv(p->n, p->L);
-  const int grid = psv::attn_grid_size(kv.data(), p->n, p->T, p->H);
+  a.n_pieces = psv::attn_pieces(kv.data(), p->n, p->T, p->H);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PSV_ECUDA;
+  const int grid = psv::attn_grid_size(a.n_pieces, sms);
   if ((e = psv::launch_attention(&tmQ, &tmK, &tmV, a, p->n, grid, st)) != cudaSuccess) return PSV_ECUDA;
   return PSV_OK;
 }

@@ -74,8 +74,29 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanh_approx(k0 * x * fmaf(0.044715f, x2, 1.0f)));
 }
 
-// Fused epilogue of 32 consecutive columns [n0, n0+32) of one row (QKV and
-// velocity head; the residual and GELU epilogues write through staged TMA boxes).
+// RoPE of 32 consecutive q or k columns of one row, starting at element e0 of
+// a head: rotate pairs (e, e+1) by angle (c*T + li) * f_{e/2}; the angle is
+// assembled from two tables built in f64 on the host.
+__device__ __forceinline__ void qk_rope32(const GemmParams& p, const TaskDev& t, int li, int e0,
+                                          float* v) {
+  const float2* rb = p.rope_base + static_cast<int64_t>(t.rope_slot) * (p.dh >> 1) + (e0 >> 1);
+  // in-chunk table is [dh/2][T]: the warp's 32 rows read 32 consecutive entries
+  const float2* rl = p.rope_local + static_cast<int64_t>(e0 >> 1) * p.T + li;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 cb = __ldg(rb + i);
+    const float2 cl = __ldg(rl + static_cast<int64_t>(i) * p.T);
+    const float cs = cb.x * cl.x - cb.y * cl.y;
+    const float sn = cb.y * cl.x + cb.x * cl.y;
+    const float a = v[2 * i], b = v[2 * i + 1];
+    v[2 * i] = a * cs - b * sn;
+    v[2 * i + 1] = a * sn + b * cs;
+  }
+}
+
+// Fused epilogue of 32 consecutive columns [n0, n0+32) of one row, written
+// row by row (velocity head; V^T and the q/k rows that qkv_chunk64 cannot
+// write as one box).
 template <int EPI>
 __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0, float* v) {
   if (row >= p.M || n0 >= p.N) return;
@@ -109,24 +130,7 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
     const int j0 = n0 - sec * p.d;
     const int head = j0 / p.dh;
     const int e0 = j0 - head * p.dh;
-    const int half = p.dh >> 1;
-    if (sec < 2) {
-      // Rotate pairs (e, e+1) by angle (c*T + li) * f_{e/2}; the angle is
-      // assembled from two tables built in f64 on the host.
-      const float2* rb = p.rope_base + static_cast<int64_t>(t.rope_slot) * half + (e0 >> 1);
-      // in-chunk table is [dh/2][T]: the warp's 32 rows read 32 consecutive entries
-      const float2* rl = p.rope_local + static_cast<int64_t>(e0 >> 1) * p.T + li;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 cb = __ldg(rb + i);
-        const float2 cl = __ldg(rl + static_cast<int64_t>(i) * p.T);
-        const float cs = cb.x * cl.x - cb.y * cl.y;
-        const float sn = cb.y * cl.x + cb.x * cl.y;
-        const float a = v[2 * i], b = v[2 * i + 1];
-        v[2 * i] = a * cs - b * sn;
-        v[2 * i + 1] = a * sn + b * cs;
-      }
-    }
+    if (sec < 2) qk_rope32(p, t, li, e0, v);
     const int ring = t.ring0 + p.block * p.S;
     const int rr = t.slot * p.T + li;  // row inside the ring
     if (sec == 2) {
@@ -249,6 +253,74 @@ __device__ __forceinline__ void gelu_chunk64(const GemmParams& p, const CUtensor
   }
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// QKV epilogue of one warp's 32 rows x 64 columns [n0, n0 + 64).  q and k
+// (bias, RoPE) are staged as a 128-byte-swizzled [32][64] bf16 box and
+// written by one TMA store: q into [rows][d] (tmq), k into the task's ring
+// rows (tmk: [rings][Lr][d]) — whole 128-byte lines instead of 32 partial
+// lines per warp store.  The box needs all 32 rows in one task and below M
+// (a box must not reach into the next task's ring rows); the few warps that
+// straddle a task boundary, and V^T (stored transposed), go row by row.
+__device__ __forceinline__ void qkv_chunk64(const GemmParams& p, const CUtensorMap* tmq,
+                                            const CUtensorMap* tmk, void* stage, int row, int row0,
+                                            int n0, float* v) {
+  if (n0 >= p.N) return;
+  const int sec = n0 / p.d;
+  const int last = row0 + 31;
+  const bool box = (p.d % 64) == 0 && sec < 2 && last < p.M && row0 / p.T == last / p.T;
+  if (!box) {
+    epilogue32<EPI_QKV>(p, row, n0, v);
+    epilogue32<EPI_QKV>(p, row, n0 + 32, v + 32);
+    return;
+  }
+  const int lane = lane_id();
+  const TaskDev& t = p.tasks[row / p.T];
+  const int li = row - t.row0;
+  const int j0 = n0 - sec * p.d;
+  uint32_t w[32];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float* vh = v + 32 * h;
+    const float4* b4 = reinterpret_cast<const float4*>(p.bias + n0 + 32 * h);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 bb = __ldg(b4 + i);
+      vh[4 * i] += bb.x;
+      vh[4 * i + 1] += bb.y;
+      vh[4 * i + 2] += bb.z;
+      vh[4 * i + 3] += bb.w;
+    }
+    const int jh = j0 + 32 * h;
+    qk_rope32(p, t, li, jh - (jh / p.dh) * p.dh, vh);
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  uint4* st4 = reinterpret_cast<uint4*>(stage);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st4[lane * 8 + (j ^ (lane & 7))] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (sec == 0) {
+      tma_store_2d(tmq, stage, j0, row0);
+    } else {
+      const TaskDev& t0 = p.tasks[row0 / p.T];
+      tma_store_3d(tmk, stage, j0, t0.slot * p.T + (row0 - t0.row0), t0.ring0 + p.block * p.S);
+    }
+    bulk_commit();
+  }
+}
+
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   int ok = 0;
@@ -260,7 +332,8 @@ template <int EPI, bool WIDE>
 __global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   using G = GemmShape<WIDE>;
   constexpr int BN = G::BN, BK = G::BK, STAGES = G::STAGES, KA = G::KA;
   constexpr int A_ATOM = G::A_ATOM, B_ATOM = G::B_ATOM, A_BYTES = G::A_BYTES, B_BYTES = G::B_BYTES;
@@ -403,14 +476,17 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
       const uint32_t tbase = tmem + acc * 256 + (static_cast<uint32_t>(q * 32) << 16);
-      if constexpr (EPI == EPI_GELU) {
+      if constexpr (EPI == EPI_GELU || EPI == EPI_QKV) {
 #pragma unroll 1
         for (int ch = chalf * (BN / 64); ch < (chalf + 1) * (BN / 64); ch += 2) {
           float v[64];
           tmem_ld32(tbase + ch * 32, v);
           tmem_ld32(tbase + ch * 32 + 32, v + 32);
           tmem_wait_ld();
-          gelu_chunk64(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+          if constexpr (EPI == EPI_GELU)
+            gelu_chunk64(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+          else
+            qkv_chunk64(p, &tmC, &tmD, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
         }
       } else {
 #pragma unroll 1
@@ -432,7 +508,7 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);  // the even CTA's barrier
     }
     // The staged stores and reductions must have completed before the CTA exits.
-    if ((EPI == EPI_RESID || EPI == EPI_GELU) && lane == 0) bulk_wait_all();
+    if ((EPI == EPI_RESID || EPI == EPI_GELU || EPI == EPI_QKV) && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -448,7 +524,7 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int EPI, bool WIDE>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
-                       const GemmParams& p, int max_ctas, cudaStream_t st) {
+                       const CUtensorMap* tmD, const GemmParams& p, int max_ctas, cudaStream_t st) {
   static int max_clusters = 0;
   const size_t smem = GemmShape<WIDE>::SMEM;
   cudaLaunchConfig_t cfg = {};
@@ -482,7 +558,7 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;  // + programmatic stream serialization
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, WIDE>, *tmA, *tmB, *tmC, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, WIDE>, *tmA, *tmB, *tmC, *tmD, p);
 }
 
 }  // namespace
@@ -497,21 +573,24 @@ size_t gemm_smem_bytes() {
 bool use_wide(int epi, int K) { return epi == EPI_RESID && K >= 4096; }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st) {
+                        const CUtensorMap* tmC, const CUtensorMap* tmD, const GemmParams& p,
+                        int grid, cudaStream_t st) {
   if ((epi == EPI_RESID || epi == EPI_GELU) && !tmC) return cudaErrorInvalidValue;
+  if (epi == EPI_QKV && p.d % 64 == 0 && (!tmC || !tmD)) return cudaErrorInvalidValue;
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
+  const CUtensorMap* dm = tmD ? tmD : tmA;
   const bool wide = use_wide(epi, p.K);
   switch (epi) {
     case EPI_QKV:
-      return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, p, grid, st)
-                  : launch_one<EPI_QKV, false>(tmA, tmB, c, p, grid, st);
+      return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, dm, p, grid, st)
+                  : launch_one<EPI_QKV, false>(tmA, tmB, c, dm, p, grid, st);
     case EPI_RESID:
-      return wide ? launch_one<EPI_RESID, true>(tmA, tmB, c, p, grid, st)
-                  : launch_one<EPI_RESID, false>(tmA, tmB, c, p, grid, st);
+      return wide ? launch_one<EPI_RESID, true>(tmA, tmB, c, dm, p, grid, st)
+                  : launch_one<EPI_RESID, false>(tmA, tmB, c, dm, p, grid, st);
     case EPI_GELU:
-      return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, p, grid, st)
-                  : launch_one<EPI_GELU, false>(tmA, tmB, c, p, grid, st);
-    case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, p, grid, st);
+      return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, dm, p, grid, st)
+                  : launch_one<EPI_GELU, false>(tmA, tmB, c, dm, p, grid, st);
+    case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, dm, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

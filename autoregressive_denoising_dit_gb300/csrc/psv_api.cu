@@ -294,6 +294,8 @@ struct psv_ctx {
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
   CUtensorMap tmC_h;  // f32 h, the target of the gated-residual TMA reductions
   CUtensorMap tmC_u;  // bf16 u, written by the GELU epilogue's TMA stores
+  CUtensorMap tmC_q;  // bf16 q and the K ring, written by the QKV epilogue's
+  CUtensorMap tmC_k;  // TMA stores (32-row x 64-column boxes)
   // executor
   bool use_graphs = true;
   std::map<int64_t, int> shape_seen;
@@ -519,7 +521,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.rope_local = ctx->at<float2>(L.rope_local);
       p.rope_base = ctx->at<float2>(L.rope_base);
       run.run(K_GEMM_QKV, 2.0 * Md * 3 * d, Md * 2 + 3.0 * d * d * 2 + 3 * Md * 2, [&] {
-        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, nullptr, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, &ctx->tmC_q, &ctx->tmC_k, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // window attention
@@ -558,7 +560,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 2 * d;
       run.run(K_GEMM_O, 2.0 * Md * d, Md * 2 + 1.0 * d * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, &ctx->tmC_h, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, &ctx->tmC_h, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // LN2 + modulation
@@ -576,7 +578,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.bias = ctx->at<float>(L.b_up) + static_cast<size_t>(b) * F;
       p.u = ctx->at<__nv_bfloat16>(L.u);
       run.run(K_GEMM_UP, 2.0 * Md * F, Md * 2 + 1.0 * F * d * 2 + static_cast<double>(M) * F * 2, [&] {
-        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, &ctx->tmC_u, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, &ctx->tmC_u, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // down + gated residual (gate2)
@@ -591,7 +593,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 5 * d;
       run.run(K_GEMM_DOWN, 2.0 * Md * F, static_cast<double>(M) * F * 2 + 1.0 * F * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, &ctx->tmC_h, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, &ctx->tmC_h, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     if (tap && b == ctx->tap_block && run.err == cudaSuccess)
@@ -611,7 +613,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     p.bias = ctx->at<float>(L.b_out);
     p.state = ctx->at<float>(L.state);
     run.run(K_GEMM_FINAL, 2.0 * Md * m.C, Md * 2 + static_cast<double>(M) * m.C * 8, [&] {
-      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, nullptr, p, gemm_grid(ctx, M, p.N), st);
+      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
     });
   }
   return run.err;
@@ -822,6 +824,13 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint64_t str[2] = {d * 2, d * 2 * L.Lr};
       uint32_t box[3] = {aw, 128, 1};
       ok &= encode_bf16(&ctx->tmK, 3, ctx->arena + L.k_ring, dims, str, box, swq);
+      if (d % 64 == 0) {
+        uint32_t obox[3] = {64, 32, 1};
+        ok &= encode_bf16(&ctx->tmC_k, 3, ctx->arena + L.k_ring, dims, str, obox, SW128);
+        uint64_t qdims[2] = {d, Mx}, qstr[1] = {d * 2};
+        uint32_t qbox[2] = {64, 32};
+        ok &= encode_bf16(&ctx->tmC_q, 2, ctx->arena + L.q, qdims, qstr, qbox, SW128);
+      }
     }
     {
       uint64_t dims[3] = {static_cast<uint64_t>(L.Lp), static_cast<uint64_t>(m.dh),

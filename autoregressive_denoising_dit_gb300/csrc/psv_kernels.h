@@ -94,9 +94,13 @@ size_t attn_smem_bytes(int dh);
 
 // tmC: output map of the epilogues that write through TMA: f32 h ([rows][d],
 // box 32 x 32, 128-byte swizzle) for EPI_RESID (TMA reduce-add), bf16 u
-// ([rows][F], box 64 x 32, 128-byte swizzle) for EPI_GELU; the others ignore it.
+// ([rows][F], box 64 x 32, 128-byte swizzle) for EPI_GELU, bf16 q ([rows][d],
+// box 64 x 32, 128-byte swizzle) for EPI_QKV; tmD: bf16 K ring ([rings][Lr][d],
+// box 64 x 32 x 1, 128-byte swizzle) for EPI_QKV (both needed when d % 64 == 0).
+// The others ignore them.
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmC, const GemmParams& p, int grid, cudaStream_t st);
+                        const CUtensorMap* tmC, const CUtensorMap* tmD, const GemmParams& p,
+                        int grid, cudaStream_t st);
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, const AttnParams& p, int n_tasks, int grid,
                              cudaStream_t st);

@@ -88,11 +88,12 @@ struct AttnCfg {
   static constexpr int OFF_BAR = OFF_V + kStages * V_BYTES;
   static constexpr int N_BARS = 12 + 4 * kStages;
   // barriers, the TMEM address word and the merge flag, two published piece
-  // slots and the softmax warps' copy (int4 each), then the row-max /
+  // slots and the softmax warps' copy (two int4 each: the piece and its task
+  // fields), then the row-max /
   // row-sum exchange area [2 key halves][128 rows] f32.  The dynamic
   // shared-memory window starts 1024-byte aligned (no static shared
   // variables; checked at run time).
-  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 3 * 16 + 2 * QT * 4;
+  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 6 * 16 + 2 * QT * 4;
   static constexpr int OH = DH / 2;              // O columns per thread
   static constexpr int OC = OH < 32 ? OH : 32;   // O columns per TMEM access
   static_assert(V_ATOM % 1024 == 0 && K_ATOM % 1024 == 0, "swizzle atoms stay 1024-aligned");
@@ -243,17 +244,23 @@ struct Piece {
   int kv_len, row0, ring;
 };
 
-__device__ __forceinline__ Piece piece_of(int4 pc, const AttnParams& p) {
+// The task fields a piece needs, published with it: {kv_len, row0, ring}.
+__device__ __forceinline__ int4 piece_task(int4 pc, const AttnParams& p) {
+  if (pc.x < 0) return make_int4(0, 0, 0, 0);
+  const TaskDev& task = p.tasks[pc.x];
+  return make_int4(task.kv_len, task.row0, task.ring0 + p.block * p.S, 0);
+}
+
+__device__ __forceinline__ Piece piece_of(int4 pc, int4 pt) {
   Piece g;
   g.ti = pc.x;
   g.head = pc.y;
   g.unit = pc.z;
   g.half = pc.w & 0xff;
   g.nsplit = pc.w >> 8;
-  const TaskDev task = p.tasks[g.ti];
-  g.kv_len = task.kv_len;
-  g.row0 = task.row0;
-  g.ring = task.ring0 + p.block * p.S;
+  g.kv_len = pt.x;
+  g.row0 = pt.y;
+  g.ring = pt.z;
   const int nt = n_key_tiles(g.kv_len);
   g.j_begin = g.half == 0 ? 0 : nt / 2;
   g.nT = ((g.nsplit == 1 || g.half == 1) ? nt : nt / 2) - g.j_begin;
@@ -341,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + VS;    // [VS] both CTAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::N_BARS);
   int* s_last_p = reinterpret_cast<int*>(tmem_slot + 1);
-  int4* pc_slot = reinterpret_cast<int4*>(tmem_slot + 4);   // [2] published pieces
-  int4* sm_piece = pc_slot + 2;                             // the softmax warps' copy
-  float* xch = reinterpret_cast<float*>(sm_piece + 1);      // [2 key halves][128 rows]
+  int4* pc_slot = reinterpret_cast<int4*>(tmem_slot + 4);   // [2][2] published pieces
+  int4* sm_piece = pc_slot + 4;                             // [2] the softmax warps' copy
+  float* xch = reinterpret_cast<float*>(sm_piece + 2);      // [2 key halves][128 rows]
 
   pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
@@ -374,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pc_empty0 = mapa_shared(pc_empty, 0);
   // A reader of the pair takes piece i from slot i & 1 and acknowledges it on
   // the even CTA (after it has used the values, so the slot may be reused).
-  auto take_piece = [&](int i, int4& pc) -> bool {
+  auto take_piece = [&](int i, int4& pc, int4& pt) -> bool {
     if (!mbar_wait_acq_cluster(&pc_full[i & 1], (i >> 1) & 1, p.err, ERR_ATTN_TIMEOUT)) return false;
-    pc = ld_shared_v4(&pc_slot[i & 1]);
+    pc = ld_shared_v4(&pc_slot[2 * (i & 1)]);
+    pt = ld_shared_v4(&pc_slot[2 * (i & 1) + 1]);
     mbar_arrive_remote(pc_empty0 + (i & 1) * 8);
     return true;
   };
@@ -393,18 +401,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_full0 = mapa_shared(k_full, 0);
         int gk = 0;
         for (int i = 0;; ++i) {
-          int4 pc;
+          int4 pc, pt;
           if (leader) {
             const int b = i & 1;
             if (i >= 2 && !mbar_wait(&pc_empty[b], ((i >> 1) - 1) & 1, p.err, ERR_ATTN_TIMEOUT)) break;
             pc = decode_piece(atomicAdd(p.counters, 1), p);
-            for (uint32_t r = 0; r < 2; ++r) st_cluster_v4(mapa_shared(&pc_slot[b], r), pc);
+            pt = piece_task(pc, p);
+            for (uint32_t r = 0; r < 2; ++r) {
+              st_cluster_v4(mapa_shared(&pc_slot[2 * b], r), pc);
+              st_cluster_v4(mapa_shared(&pc_slot[2 * b + 1], r), pt);
+            }
             for (uint32_t r = 0; r < 2; ++r) mbar_arrive_cluster(mapa_shared(&pc_full[b], r));
-          } else if (!take_piece(i, pc)) {
+          } else if (!take_piece(i, pc, pt)) {
             break;
           }
           if (pc.x < 0) break;
-          const Piece pg = piece_of(pc, p);
+          const Piece pg = piece_of(pc, pt);
           // The Q buffer is reused once the previous piece's S MMAs are done.
           if (i > 0 && !mbar_wait(q_empty, (i - 1) & 1, p.err, ERR_ATTN_TIMEOUT)) break;
           if (leader) mbar_arrive_expect_tx(q_full, 2 * Cfg::Q_BYTES);
@@ -443,9 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_full0 = mapa_shared(v_full, 0);
         int gv = 0;
         for (int i = 0;; ++i) {
-          int4 pc;
-          if (!take_piece(i, pc) || pc.x < 0) break;
-          const Piece pg = piece_of(pc, p);
+          int4 pc, pt;
+          if (!take_piece(i, pc, pt) || pc.x < 0) break;
+          const Piece pg = piece_of(pc, pt);
           bool ok = true;
           for (int j = 0; j < pg.nT; ++j, ++gv) {
             const int st = gv % VS;
@@ -496,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // tiles of earlier pieces
       bool ok = true;
       for (int i = 0; ok; ++i) {
-        int4 pc;
-        if (!take_piece(i, pc) || pc.x < 0) break;
-        const int nT = piece_of(pc, p).nT;
+        int4 pc, pt;
+        if (!take_piece(i, pc, pt) || pc.x < 0) break;
+        const int nT = piece_of(pc, pt).nT;
         if (!mbar_wait(q_full, i & 1, p.err, ERR_ATTN_TIMEOUT) ||
             !mbar_wait(&k_full[g % KS], (g / KS) & 1, p.err, ERR_ATTN_TIMEOUT) ||
             (g > 0 && !mbar_wait(s_free, (g - 1) & 1, p.err, ERR_ATTN_TIMEOUT)))
@@ -576,14 +588,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // error, which ends the loop for all).  The copy is rewritten only after
       // every warp has passed this piece's later barriers.
       if (warp == 4 && lane == 0) {
-        int4 pc;
-        if (!take_piece(i, pc)) pc.x = -1;
-        *sm_piece = pc;
+        int4 pc, pt;
+        if (!take_piece(i, pc, pt)) pc.x = -1;
+        sm_piece[0] = pc;
+        sm_piece[1] = pt;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const int4 pc = ld_shared_v4(sm_piece);
       if (pc.x < 0) break;
-      const Piece pg = piece_of(pc, p);
+      const Piece pg = piece_of(pc, ld_shared_v4(sm_piece + 1));
       const int nT = pg.nT;
       float m = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
       bool ok = true;

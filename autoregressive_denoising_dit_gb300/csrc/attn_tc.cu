@@ -276,6 +276,13 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, int4 v) {
                : "memory");
 }
 
+// One 32-byte global store (a whole sector); ptr 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ int4 ld_shared_v4(const void* ptr) {
   int4 v;
   asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
@@ -713,16 +720,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = (qloc0 + r) < p.T;
       __nv_bfloat16* dst = p.o + static_cast<int64_t>(pg.row0 + qloc0 + r) * p.d + pg.head * DH +
                            hk * Cfg::OH;
+      // 32-byte stores (whole sectors) where O rows are 32-byte aligned.
+      const bool o32 = ((reinterpret_cast<uintptr_t>(p.o) | (static_cast<uintptr_t>(p.d) * 2)) & 31) == 0;
       auto store_row = [&](const float* v, int c, float inv) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * Cfg::OC);
+        uint32_t w[Cfg::OC / 2];
 #pragma unroll
-        for (int e = 0; e < Cfg::OC / 8; ++e) {
-          uint4 w;
-          w.x = pack_bf16x2(v[8 * e + 0] * inv, v[8 * e + 1] * inv);
-          w.y = pack_bf16x2(v[8 * e + 2] * inv, v[8 * e + 3] * inv);
-          w.z = pack_bf16x2(v[8 * e + 4] * inv, v[8 * e + 5] * inv);
-          w.w = pack_bf16x2(v[8 * e + 6] * inv, v[8 * e + 7] * inv);
-          d4[e] = w;
+        for (int e = 0; e < Cfg::OC / 2; ++e) w[e] = pack_bf16x2(v[2 * e] * inv, v[2 * e + 1] * inv);
+        if (o32) {
+#pragma unroll
+          for (int e = 0; e < Cfg::OC / 16; ++e) st_global_v8(dst + c * Cfg::OC + 16 * e, w + 8 * e);
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * Cfg::OC);
+#pragma unroll
+          for (int e = 0; e < Cfg::OC / 8; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
         }
       };
       if (pg.nsplit == 1) {

@@ -73,6 +73,7 @@ CASES = [
     dict(n=3, T=300, H=4, dh=64, L=2100, k_rows=2200, vt_cols=2240),   # ragged, tail query unit
     dict(n=1, T=64, H=4, dh=32, L=256),                                # dh = 32 (64-byte swizzle)
     dict(n=2, T=1560, H=2, dh=128, L=7800),                            # full-size window
+    dict(n=8, T=300, H=8, dh=64, L=2100),                              # 192 work pieces > 76 pairs
     dict(n=2, T=300, H=2, dh=64, L=16500, k_rows=16600, vt_cols=16512),  # split, ragged last tile
     dict(n=2, T=130, H=1, dh=128, L=1),                                # single key
 ]

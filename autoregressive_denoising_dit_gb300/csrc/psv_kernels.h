@@ -63,11 +63,11 @@ struct AttnParams {
 };
 
 // Key tiles (of 256) from which a (task, head, query unit) is split in two
-// halves processed by two CTA pairs; depends on the task's kv_len only, so
-// the result of a task does not depend on the rest of the wave.  Splitting
-// doubles the work items and adds a merge through global memory; measured on
-// the 1.3B wave (7800-key windows), not splitting is 12% faster, so only
-// windows of 16K keys and more are split.
+// key halves (two work pieces, merged through global memory); the split
+// depends on the task's kv_len and on the unit being a tail only, so the
+// result of a task does not depend on the rest of the wave.  Splitting every
+// 7800-key window of the 1.3B wave made the attention 12% slower (twice the
+// pieces and a merge), so only windows of 16K keys and more are split.
 constexpr int kAttnSplitMinTiles = 64;
 // Tail units (the last query unit of a task when its rows fit in one CTA,
 // e.g. 24 of T = 1560) cost as much as a full unit; from this many key tiles

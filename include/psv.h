@@ -271,7 +271,8 @@ int psv_debug_read_kv(psv_ctx* ctx, int stream_id, int block, int step,
  * Requirements: dh in {32, 64, 128}; H*dh % 8 == 0; 1 <= L <= k_rows;
  * L <= vt_cols, vt_cols % 8 == 0; all pointers 16-byte aligned device memory.
  * scratch: caller-owned device memory of at least psv_attention_scratch_bytes
- * bytes (task table, split-key partials, arrival counters), 256-byte aligned;
+ * bytes (task table, the work queue of the persistent CTA pairs and the
+ * split-key arrival counters, split-key partials), 256-byte aligned;
  * it is overwritten and must not be shared by calls that may overlap on the
  * GPU.  Asynchronous on cuda_stream; the int at the start of scratch is set
  * nonzero if a device-side pipeline wait timed out.  Errors: PSV_EINVAL. */

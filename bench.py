@@ -491,9 +491,11 @@ def run_latency(args, cfg_name, cfg, world, rank, local):
     next_chunk = n_chunks
     e2e = []
     for k in range(args.steps + 2):
+        # the chunk's input is made before its clock starts (as in the wave e2e)
+        noise = [np.ascontiguousarray(st.noise(next_chunk), dtype=np.float32) for st in streams]
         w0 = time.perf_counter()
-        for st, sid in zip(streams, sids):
-            sess.submit(sid, st.noise(next_chunk))
+        for x, sid in zip(noise, sids):
+            sess.submit(sid, x)
         for _ in range(S):
             sess.run_wave()
         for sid in sids:

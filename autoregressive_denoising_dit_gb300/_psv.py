@@ -48,7 +48,7 @@ EXPORTS = [
     "psv_destroy", "psv_last_error",
     "psv_set_graphs", "psv_set_profiling", "psv_kernel_times", "psv_debug_tap",
     "psv_debug_read_kv", "psv_attention_scratch_bytes", "psv_attention",
-    "psv_attention_noalloc",
+    "psv_attention_noalloc", "psv_attention_noalloc_status", "psv_debug_error_word",
 ]
 
 PSV_ATTN_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -127,6 +127,8 @@ def lib() -> ctypes.CDLL:
             "psv_attention_scratch_bytes": (i32, [ctypes.POINTER(AttnProblem), ctypes.POINTER(sz)]),
             "psv_attention": (i32, [ctypes.POINTER(AttnProblem), vp, vp, vp, vp, vp, sz, vp]),
             "psv_attention_noalloc": (i32, [ctypes.POINTER(AttnProblem), vp, vp, vp, vp, vp]),
+            "psv_attention_noalloc_status": (i32, [ctypes.POINTER(i32), vp]),
+            "psv_debug_error_word": (i32, [vp, ctypes.POINTER(sz)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -307,6 +309,13 @@ def psv_debug_read_kv(ctx, sid: int, block: int, step: int, rows: int, d: int):
     return k, v
 
 
+def psv_debug_error_word(ctx) -> int:
+    """Byte offset of the device error word within the context's arena."""
+    off = ctypes.c_size_t()
+    _check(ctx, lib().psv_debug_error_word(ctx, ctypes.byref(off)))
+    return off.value
+
+
 def psv_attention_scratch_bytes(prob: AttnProblem) -> int:
     n = ctypes.c_size_t()
     _check(None, lib().psv_attention_scratch_bytes(ctypes.byref(prob), ctypes.byref(n)))
@@ -334,3 +343,13 @@ def psv_attention_noalloc(prob: AttnProblem, q_ptr: int, k_ptr: int, vt_ptr: int
                           f"fixed {PSV_ATTN_NOALLOC_SCRATCH_BYTES >> 20} MiB array holds")
     if r < 0:
         raise PSVError(r, "psv_attention_noalloc rejected its arguments (shape or alignment)")
+
+
+def psv_attention_noalloc_status(stream_ptr: int = 0) -> int:
+    """Error word of the last psv_attention_noalloc call on the current device
+    (waits for the stream first): 0, or nonzero if a device-side wait timed out."""
+    st = ctypes.c_int()
+    r = lib().psv_attention_noalloc_status(ctypes.byref(st), ctypes.c_void_p(stream_ptr or None))
+    if r < 0:
+        raise PSVError(r, "psv_attention_noalloc_status failed")
+    return st.value

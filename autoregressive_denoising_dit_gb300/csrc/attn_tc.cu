@@ -823,21 +823,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DH>
 cudaError_t launch_dh(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                       const AttnParams& p, int grid, cudaStream_t st) {
-  static bool attr_set = false;
+  static uint64_t set_up = 0;
   const size_t smem = attn_smem_bytes(DH);
-  if (!attr_set) {
+  cudaError_t e = once_per_device(&set_up, [&](int) {
     // The register split must fit the launch allocation, else the growing
     // warpgroups would wait for registers forever.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel<DH>);
-    if (e != cudaSuccess) return e;
+    cudaError_t r = cudaFuncGetAttributes(&fa, attn_tc_kernel<DH>);
+    if (r != cudaSuccess) return r;
     if (fa.numRegs * kThreads < kRegsNeeded || fa.numRegs < kRegsLow || fa.numRegs > kRegsHigh)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return cudaFuncSetAttribute(attn_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -910,6 +909,10 @@ int attn_pieces(const int* kv_lens, int n_tasks, int T, int H) {
   int total = 0;
   for (int t = 0; t < n_tasks; ++t) total += pieces_main(kv_lens[t], T, H) + pieces_tail(kv_lens[t], T, H);
   return total;
+}
+
+int attn_pieces_uniform(int L, int n_tasks, int T, int H) {
+  return n_tasks * (pieces_main(L, T, H) + pieces_tail(L, T, H));
 }
 
 int attn_grid_size(int n_pieces, int sm_count) {

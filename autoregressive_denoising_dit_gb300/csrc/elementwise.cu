@@ -267,13 +267,12 @@ cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat1
                                cudaStream_t st) {
   if (R < 1 || R > 8 || K % 8 != 0) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(R) * K * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(cond_linear_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static uint64_t set_up = 0;
+  cudaError_t e = once_per_device(&set_up, [](int) {
+    return cudaFuncSetAttribute(cond_linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                200 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int warps = CL_THREADS / 32;
   cond_linear_kernel<<<(N + warps - 1) / warps, CL_THREADS, smem, st>>>(in, R, K, W, b, add, out,

@@ -525,7 +525,8 @@ __global__ void __launch_bounds__(320, 1)
 template <int EPI, bool WIDE>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                        const CUtensorMap* tmD, const GemmParams& p, int max_ctas, cudaStream_t st) {
-  static int max_clusters = 0;
+  static uint64_t set_up = 0;
+  static int max_clusters_dev[64] = {};
   const size_t smem = GemmShape<WIDE>::SMEM;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -540,18 +541,23 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, WIDE>,
+  cudaError_t e = once_per_device(&set_up, [&](int dev) {
+    cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<EPI, WIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    if (r != cudaSuccess) return r;
     cfg.gridDim = dim3(2);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI, WIDE>, &cfg);
-    if (e != cudaSuccess) return e;
+    r = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<EPI, WIDE>, &cfg);
+    if (r != cudaSuccess) return r;
     if (n < 1) return cudaErrorInvalidConfiguration;
-    max_clusters = n;
-  }
+    max_clusters_dev[dev] = n;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  const int max_clusters = max_clusters_dev[dev];
   const int n_m = (p.M + BM - 1) / BM, n_n = (p.N + GemmShape<WIDE>::BN - 1) / GemmShape<WIDE>::BN;
   const int n_pt = ((n_m + 1) / 2) * n_n;
   int clusters = max_clusters < n_pt ? max_clusters : n_pt;

@@ -1374,6 +1374,13 @@ PSV_API int psv_debug_tap(psv_ctx* ctx, int block, float* h_in, float* h_out) {
   return PSV_OK;
 }
 
+PSV_API int psv_debug_error_word(psv_ctx* ctx, size_t* arena_offset) {
+  if (!ctx || !arena_offset) return PSV_EINVAL;
+  if (ctx->plan_only) return set_err(ctx, PSV_EINVAL, "plan-only context has no error word");
+  *arena_offset = ctx->L.err;
+  return PSV_OK;
+}
+
 PSV_API int psv_debug_read_kv(psv_ctx* ctx, int sid, int block, int step, float* k, float* v) {
   if (int r = check_ctx(ctx)) return r;
   const psv_model_desc& m = ctx->m;

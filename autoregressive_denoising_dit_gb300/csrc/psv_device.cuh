@@ -125,19 +125,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// TMA load multicast to the CTAs of the cluster in cta_mask: each receives
-// the box at the same shared-memory offset and a complete_tx on its own
-// barrier at the same offset.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int x, int y, int z, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is signalled on a
 // barrier of either CTA of the CTA pair (bar_cluster: shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,

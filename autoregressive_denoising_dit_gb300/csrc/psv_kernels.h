@@ -7,7 +7,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace psv {
+
+// Runs the set-up step f (function attributes, occupancy queries) once per
+// CUDA device, for the device current at the call: an attribute set on one
+// device does not carry over to another.  `done` is the caller's bit mask of
+// devices already set up (devices 0..63); one lock serialises every set-up.
+inline std::mutex& device_setup_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+template <class F>
+cudaError_t once_per_device(uint64_t* done, F&& f) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(device_setup_mutex());
+  if ((*done >> dev) & 1u) return cudaSuccess;
+  e = f(dev);
+  if (e == cudaSuccess) *done |= uint64_t{1} << dev;
+  return e;
+}
 
 struct TaskDev;
 
@@ -80,6 +103,8 @@ int attn_units(int T);
 // Work pieces (256 query rows x a whole window or one key half) of a launch
 // over these kv lengths.
 int attn_pieces(const int* kv_lens, int n_tasks, int T, int H);
+// The same for n tasks that all attend to L keys.
+int attn_pieces_uniform(int L, int n_tasks, int T, int H);
 // CTAs (two per pair) of a persistent launch: one pair per two SMs at most.
 int attn_grid_size(int n_pieces, int sm_count);
 size_t attn_part_floats(int max_tasks, int T, int H, int dh);

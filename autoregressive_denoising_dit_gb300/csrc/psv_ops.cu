@@ -7,7 +7,6 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
-#include <vector>
 
 #include "../../include/psv.h"
 #include "psv_device.cuh"
@@ -109,8 +108,7 @@ int psv_attention_enqueue(const psv_attn_problem* p, const void* q, const void* 
   a.counters = reinterpret_cast<int*>(scratch + L.counters);
   a.max_pairs = psv::attn_units(p->T);
   a.err = reinterpret_cast<int*>(scratch + L.err);
-  std::vector<int> kv(p->n, p->L);
-  a.n_pieces = psv::attn_pieces(kv.data(), p->n, p->T, p->H);
+  a.n_pieces = psv::attn_pieces_uniform(p->L, p->n, p->T, p->H);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -142,9 +140,12 @@ PSV_API int psv_attention(const psv_attn_problem* p, const void* q, const void* 
 // they call: a control loop that must never enter the CUDA allocator after
 // start-up (its latency and failure modes are not bounded), or a host
 // framework that owns every device allocation and hands out no scratch.  For
-// them the scratch of the attention call lives in this file-scope array,
-// which the CUDA module reserves once per device when the library is loaded
-// and keeps until the process exits.
+// them the scratch of the attention call lives in this file-scope array.
+// The CUDA module that holds it is loaded on a device, and the array
+// reserved there until the process exits, when the module is first used on
+// that device: with CUDA's default lazy module loading that is the set-up of
+// the first call below.  Nothing on the call path allocates host or device
+// memory after that set-up.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = PSV_ATTN_NOALLOC_SCRATCH_BYTES;
@@ -152,6 +153,22 @@ static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchByt
 
 std::mutex g_scratch_mu;
 char* g_scratch_ptr[64] = {};  // device address of g_attn_scratch, per device
+
+// Device address of the array on the current device, looked up once per
+// device with that device current: in host code the name g_attn_scratch is
+// only a host-side stand-in, which a kernel must never be given.
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PSV_ECUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) return PSV_ECUDA;
+    g_scratch_ptr[dev] = static_cast<char*>(ptr);
+  }
+  *out = g_scratch_ptr[dev];
+  return PSV_OK;
+}
 
 }  // namespace
 
@@ -161,20 +178,18 @@ PSV_API int psv_attention_noalloc(const psv_attn_problem* p, const void* q, cons
   if (!q || !k || !vt || !o) return PSV_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o)) return PSV_EINVAL;
   if (attn_scratch_layout(*p).total > kNoAllocScratchBytes) return PSV_ENOMEM;  // over the fixed size
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PSV_ECUDA;
   char* scratch = nullptr;
-  {
-    // Set-up on the first call on each device, with that device current: the
-    // host-side name g_attn_scratch is only a stand-in, the kernel needs the
-    // device address.
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-      void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) return PSV_ECUDA;
-      g_scratch_ptr[dev] = static_cast<char*>(ptr);
-    }
-    scratch = g_scratch_ptr[dev];
-  }
+  if (int r = noalloc_scratch(&scratch)) return r;
   return psv_attention_enqueue(p, q, k, vt, o, scratch, static_cast<cudaStream_t>(cuda_stream));
+}
+
+PSV_API int psv_attention_noalloc_status(int* status, void* cuda_stream) {
+  if (!status) return PSV_EINVAL;
+  char* scratch = nullptr;
+  if (int r = noalloc_scratch(&scratch)) return r;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // The error word sits at the start of the array (offset 0 of the layout).
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PSV_ECUDA;
+  if (cudaMemcpy(status, scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PSV_ECUDA;
+  return PSV_OK;
 }

@@ -137,10 +137,16 @@ typedef struct psv_kernel_time {
 typedef struct psv_ctx psv_ctx;
 
 /* Device bytes psv_create needs for this description (weights, KV rings
- * for max_streams, activations for the largest wave, latent state, tables). */
+ * for max_streams, activations for the largest wave, latent state, tables):
+ * the memory footprint a stream placement checks against (AREX article,
+ * section 三层设计, third layer: a stream is admitted only if it fits). */
 int psv_arena_bytes(const psv_model_desc* desc, size_t* bytes);
 
-/* Create a context.  dev_arena/arena_bytes: caller-owned device memory of at
+/* Create a context: one served model on one GPU, whose device memory holds
+ * the model's weights, every stream's noisy-KV rings and the activations of
+ * the largest wave (AREX article, section 三层设计, second layer: one GPU
+ * time-shares the stages of many (block, step) pairs and keeps their state).
+ * dev_arena/arena_bytes: caller-owned device memory of at
  * least psv_arena_bytes() bytes, 1024-byte aligned, used until psv_destroy;
  * cuda_stream: caller-owned cudaStream_t all device work is issued on
  * (NULL = legacy default stream).  With PSV_FLAG_PLAN_ONLY the arena and
@@ -149,12 +155,19 @@ int psv_arena_bytes(const psv_model_desc* desc, size_t* bytes);
 int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena_bytes,
                void* cuda_stream, psv_ctx** out);
 
-/* Copy n tensors into the arena (see the weight table above).  Synchronous
+/* Copy n tensors into the arena (see the weight table above).  The model is
+ * served as loaded: unpruned, uncompressed, unquantised weights (AREX article,
+ * section 实测数字), here bf16 matrices and f32 biases.  Synchronous
  * with respect to the host buffers.  Errors: PSV_EINVAL (unknown id, wrong
  * numel or dtype), PSV_ECUDA. */
 int psv_load_weights(psv_ctx* ctx, const psv_weight* w, int n);
 
-/* Open a stream with conditioning vector cond (host, f32 [d]).  Builds the
+/* Open a stream: one agent's sequence of chunks, generated autoregressively
+ * and conditioned on that agent (AREX article, section 难题: an
+ * action-conditioned world model generates the next frames from the current
+ * observation and action; section 三层设计, third layer: each stream is
+ * scheduled as a unit).  cond: the stream's conditioning vector (host, f32
+ * [d]).  Builds the
  * stream's adaLN tables on the device: for every step s,
  * e_s = T2 SiLU(T1 emb(t_s) + b1) + b2 + cond, mod[s][b] = MOD_W,b SiLU(e_s)
  * + MOD_B,b, fmod[s] = FMOD_W SiLU(e_s) + FMOD_B.  Stream ids are assigned
@@ -162,7 +175,11 @@ int psv_load_weights(psv_ctx* ctx, const psv_weight* w, int n);
 int psv_open_stream(psv_ctx* ctx, const float* cond, int* stream_id);
 
 /* Submit the next chunk of a stream: noise (host, f32 [T, C], the chunk's
- * x_0).  Chunks are numbered 0, 1, ... in submission order.  Errors:
+ * x_0).  Every chunk starts from pure noise and is denoised over S steps;
+ * it may start before its predecessor has finished, reading at each step the
+ * predecessor's still-noisy KV of that step (BAAI announcement, section
+ * 新一代物理 AI 的基础设施, Fig. 1 right).  Chunks are numbered 0, 1, ... in
+ * submission order.  Errors:
  * PSV_EAGAIN (max_inflight chunks alive: poll first), PSV_EINVAL. */
 int psv_submit_chunk(psv_ctx* ctx, int stream_id, const float* noise);
 
@@ -179,26 +196,42 @@ int psv_submit_chunk(psv_ctx* ctx, int stream_id, const float* noise);
 int psv_submit_chunk_cond(psv_ctx* ctx, int stream_id, const float* noise, const float* cond);
 
 /* Run one wave: every task whose dependencies are met, all streams batched
- * block by block.  Asynchronous on the context stream.  *n_tasks = tasks
- * run (0 = nothing ready; no device work issued). */
+ * block by block.  The tasks that sit on the same transformer block, from
+ * different chunks, denoising steps and streams, run as one batch, so that
+ * weight loads and kernel launches are shared (AREX article, section 三层设计,
+ * second layer; BAAI announcement, section PhysisServe, time-sharing and
+ * Fig. 3 right, cross-stream batching on one card).  Asynchronous on the
+ * context stream.  *n_tasks = tasks run (0 = nothing ready; no device work
+ * issued). */
 int psv_run_wave(psv_ctx* ctx, int* n_tasks);
 
-/* Return the oldest finished, not yet returned chunk of a stream: copies
+/* Return the oldest finished, not yet returned chunk of a stream, in chunk
+ * order: the stream's output, one chunk per steady interval (BAAI
+ * announcement, Fig. 1 right and Fig. 2: once the pipeline is full a new
+ * chunk comes out every interval; AREX article, section 实测数字: the output
+ * latency is that interval).  Copies
  * its final latent x_S (f32 [T, C]) to host `out` and its index to
  * *chunk_idx.  Non-blocking: PSV_EAGAIN if that chunk's wave has not
  * finished on the device (or no chunk of the stream has been run to its
  * last step).  Checks the device error word: PSV_EDEVICE if set. */
 int psv_poll_chunk(psv_ctx* ctx, int stream_id, float* out, int64_t* chunk_idx);
 
-/* Wait (host-side polling, no device spin) until all issued work is done.
+/* Wait (host-side polling, no device spin) until all issued work is done:
+ * the end of the time slices issued so far on the one time-shared GPU
+ * (AREX article, section 三层设计, second layer).
  * timeout_ms < 0 waits without deadline.  PSV_ETIMEDOUT on deadline. */
 int psv_sync(psv_ctx* ctx, int timeout_ms);
 
-/* The task list the next psv_run_wave would run (no state change).
+/* The task list the next psv_run_wave would run (no state change): the
+ * ready (stream, chunk, step) tasks of the dependency DAG of the pages
+ * (BAAI announcement, Fig. 2, upper part: one row per stage, one column per
+ * chunk).
  * Writes min(n, cap) entries; *n = number of ready tasks. */
 int psv_wave_plan(psv_ctx* ctx, psv_task* buf, int cap, int* n);
 
-/* Close a stream; its id and rings become free.  Queued work is not
+/* Close a stream; its id and rings become free for a later stream (AREX
+ * article, section 三层设计, third layer: streams arrive and leave while
+ * others keep running).  Queued work is not
  * cancelled: call after its chunks were polled. */
 int psv_close_stream(psv_ctx* ctx, int stream_id);
 
@@ -229,11 +262,14 @@ int psv_predict_wave_ms(psv_ctx* ctx, int n_streams, double* ms);
 int psv_admit_stream(psv_ctx* ctx, const float* cond, double slo_ms, int* stream_id,
                      double* predicted_ms);
 
-/* Destroy the context (synchronises the stream first).  NULL is a no-op. */
+/* Destroy the context (synchronises the stream first); the arena returns to
+ * the caller.  NULL is a no-op.  (Housekeeping: the pages have no
+ * counterpart.) */
 void psv_destroy(psv_ctx* ctx);
 
 /* Last error message of this context ("" if none); NULL ctx gives the
- * message of the last failed psv_create. */
+ * message of the last failed psv_create.  (Housekeeping: the pages have no
+ * counterpart.) */
 const char* psv_last_error(const psv_ctx* ctx);
 
 /* ---- executor controls and introspection -------------------------------- */
@@ -257,6 +293,14 @@ int psv_debug_tap(psv_ctx* ctx, int block, float* h_in, float* h_out);
  * k [(W+1)*T, d] and v [(W+1)*T, d], rows = slot*T + token.  Synchronous. */
 int psv_debug_read_kv(psv_ctx* ctx, int stream_id, int block, int step,
                       float* k, float* v);
+
+/* Debug: byte offset, from the start of the arena given to psv_create, of
+ * the int error word that a kernel sets when a device-side wait times out or
+ * a bounds check fails (psv_poll_chunk and psv_sync then return the sticky
+ * PSV_EDEVICE).  Lets a test raise the word from the host, without any
+ * kernel fault, to check that path.  Errors: PSV_EINVAL (plan-only
+ * context). */
+int psv_debug_error_word(psv_ctx* ctx, size_t* arena_offset);
 
 /* ---- kernel-level window attention ---------------------------------------
  * The attention step of the wave (AREX article "vLLM 与 Physis-AI 联合介绍
@@ -290,20 +334,29 @@ int psv_attention(const psv_attn_problem* p, const void* q, const void* k, const
  * allocator after start-up, or a host framework that owns all device memory
  * and provides no scratch.  Same arguments and results as psv_attention,
  * without scratch: the library uses a fixed array of
- * PSV_ATTN_NOALLOC_SCRATCH_BYTES bytes that the CUDA module reserves on every
- * device that loads libpsv and keeps until the process exits.  Problems
+ * PSV_ATTN_NOALLOC_SCRATCH_BYTES bytes inside its CUDA module, which every
+ * device that loads the module holds until the process exits.  Problems
  * whose scratch (psv_attention_scratch_bytes) exceeds that size are rejected
- * with PSV_ENOMEM; bad shapes or pointers with PSV_EINVAL.  The call
- * allocates nothing.  Its first call on a device
- * looks up the array's device address (with that device current), so make
- * that first call before any stream capture.  Every call shares the one
- * array (the call clears the parts that must start at zero); calls whose
- * work may overlap on the GPU race on it and must be ordered by the caller
- * (e.g. issued on one stream).  Device-side pipeline timeouts are recorded
- * in the shared array, not returned. */
+ * with PSV_ENOMEM; bad shapes or pointers with PSV_EINVAL.
+ * Set-up: the first call on a device, with that device current, looks up
+ * the array's device address.  Under CUDA's default lazy module loading that
+ * is also when the module is loaded on the device and the array reserved, so
+ * the first call may fail with PSV_ECUDA if the device is out of memory; make
+ * it at start-up, and before any stream capture.  Later calls allocate
+ * nothing, on the host or on the device.  Every call shares the one array
+ * (each call clears the parts that must start at zero), and the array keeps
+ * the last call's contents; calls whose work may overlap on the GPU race on
+ * it and must be ordered by the caller (e.g. issued on one stream). */
 #define PSV_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 int psv_attention_noalloc(const psv_attn_problem* p, const void* q, const void* k,
                           const void* vt, void* o, void* cuda_stream);
+
+/* Status of the last psv_attention_noalloc call on the current device:
+ * waits for cuda_stream, then *status = the error word of the shared array
+ * (0, or nonzero if a device-side pipeline wait of that call timed out and
+ * its output is not valid).  Allocates nothing.  Errors: PSV_EINVAL,
+ * PSV_ECUDA. */
+int psv_attention_noalloc_status(int* status, void* cuda_stream);
 
 #ifdef __cplusplus
 }

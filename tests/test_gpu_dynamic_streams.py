@@ -2,13 +2,15 @@
 mid-run (psv_admit_stream / psv_close_stream) do not disturb the streams
 already running, and a reused ring set starts clean.  Batch invariance makes
 this exact: every stream's outputs equal, bit for bit, a run of that stream
-alone.  The admission model's prediction after timed steady waves comes from
-the measured wave time."""
+alone, and they match the oracle (which runs each stream by itself) within
+the end-to-end tolerance, rel-L2 <= 3e-2 on the final latent and on its
+displacement.  The admission model's prediction after timed steady waves
+comes from the measured wave time."""
 import numpy as np
 import pytest
 
 import synth
-from _harness import gpu_session
+from _harness import gpu_session, rel_l2, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -78,9 +80,13 @@ def test_streams_admitted_and_closed_mid_run(name):
         sess.close()
     for got, st in ((out[a], sa), (out[b], sb), (out_c, sc)):
         ref = _alone(cfg, w, st, n)
+        ora = run_oracle(cfg, w, [st], n)[0]
         assert len(got) == n
         for c in range(n):
             assert np.array_equal(got[c], ref[c]), c
+            x0 = st.noise(c).astype(np.float64)
+            assert rel_l2(got[c], ora[c]) <= 3e-2, c
+            assert rel_l2(got[c] - x0, ora[c] - x0) <= 3e-2, c
 
 
 def test_prediction_uses_measured_steady_waves():

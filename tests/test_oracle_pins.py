@@ -438,3 +438,97 @@ def test_chunk_conditioning_is_causal():
         assert np.array_equal(base[c], moved[c])
     for c in (2, 3, 4):
         assert np.max(np.abs(base[c] - moved[c])) > 1e-6
+
+
+# ------------------------------------------------------------ final head, positions
+
+def test_final_velocity_closed_form():
+    """Final adaLN + head (reading <5>) on rows whose LayerNorm is known
+    exactly: row r = mu_r + sigma_r * z with z = (+1, -1, +1, ...), so the
+    row has mean mu_r, biased variance sigma_r^2 and LN(row) = z * sigma_r /
+    sqrt(sigma_r^2 + eps).  The head reads column 2j+1 into output j
+    (W_out[j, 2j+1] = 1), shift_f and scale_f are different constants and
+    b_out is a ramp, so a swapped [shift_f, scale_f] split, a missing LN, an
+    LN without the eps, a transposed or shifted head or a dropped bias gives
+    another value."""
+    d, C, eps = 16, 5, 1e-6
+    cfg = {"d": d, "ln_eps": eps}
+    z = np.array([1.0 if e % 2 == 0 else -1.0 for e in range(d)])
+    mus, sigmas = [3.0, -0.5, 0.0], [2.0, 0.25, 1e-3]
+    h = np.stack([m + s * z for m, s in zip(mus, sigmas)])
+    shift_c, scale_c = 0.75, -0.4
+    fmod = np.concatenate([np.full(d, shift_c), np.full(d, scale_c)])
+    out_w = np.zeros((C, d))
+    for j in range(C):
+        out_w[j, 2 * j + 1] = 1.0
+    out_b = np.arange(C) * 0.1
+    g = {"out_w": out_w, "out_b": out_b}
+    v = M.final_velocity(cfg, g, fmod, h)
+    for r, s in enumerate(sigmas):
+        ln_odd = -s / math.sqrt(s * s + eps)  # z = -1 on every odd column
+        expect = [ln_odd * (1.0 + scale_c) + shift_c + out_b[j] for j in range(C)]
+        np.testing.assert_allclose(v[r], expect, rtol=0, atol=1e-12)
+
+
+def test_final_velocity_uses_its_step_fmod_in_the_runner():
+    """Inside a run the head uses the fmod row of the task's own step: with
+    identity blocks (zero adaLN weights, so zero gates) and a head that reads
+    the modulated LN of h, only shift_f enters through b_fmod, which makes the
+    velocity of every step the same constant and x_S = x_0 - (shift_f . head
+    + b_out) in closed form, step by step."""
+    cfg = _tiny_cfg(S=4, B=1)
+    w = synth.make_weights(cfg, 0)
+    d, C = cfg["d"], cfg["C"]
+    for bw in w["blocks"]:
+        bw["mod_w"] = np.zeros_like(bw["mod_w"])
+        bw["mod_b"] = np.zeros_like(bw["mod_b"])
+    # fmod = b_fmod whatever the step: shift_f = 0.5, scale_f = -1 (zeroes the LN term)
+    w["global"]["fmod_w"] = np.zeros_like(w["global"]["fmod_w"])
+    w["global"]["fmod_b"] = np.concatenate([np.full(d, 0.5), np.full(d, -1.0)]).astype(np.float32)
+    head = np.random.default_rng(21).standard_normal((C, d)).astype(np.float32)
+    w["global"]["out_w"] = head
+    w["global"]["out_b"] = np.zeros(C, np.float32)
+    r, st = _runner(cfg, w)
+    x0 = st[0].noise(0).astype(np.float64)
+    r.submit(0, st[0].noise(0))
+    r.run_until_idle()
+    vel = np.array([0.5 * head[j].astype(np.float64).sum() for j in range(C)])
+    np.testing.assert_allclose(r.streams[0].outputs[0], x0 - vel[None, :], rtol=0, atol=1e-12)
+
+
+def test_positions_offset_each_chunk_by_T():
+    """RoPE positions are global, c*T + i (the configurations' definition).
+    Three chunks with the same noise give the same pre-RoPE keys at block 0,
+    step 0 (their block input depends only on their own x_0), so the stored
+    keys of chunk c must equal chunk 0's keys with pair j of every head turned
+    by the extra angle c*T*theta^(-2j/dh), checked as a complex product, and
+    chunk 0's keys must be its un-rotated keys turned by i*theta^(-2j/dh).
+    An offset of c*(T-1), (c+1)*T or none fails it."""
+    cfg = _tiny_cfg(W=2, B=1, S=1)
+    w = synth.make_weights(cfg, 0)
+    T, H, dh, theta = cfg["T"], cfg["H"], cfg["dh"], cfg["rope_theta"]
+    st = synth.make_streams(cfg, 1)[0]
+    r = OracleRunner(cfg, w)
+    r.open_stream(st.cond)
+    for _ in range(3):
+        r.submit(0, st.noise(0))
+    r.run_until_idle()
+    k0 = r.streams[0].kv[(0, 0, 0)][0]
+
+    def as_complex(k):
+        kr = k.reshape(T, H, dh // 2, 2)
+        return kr[..., 0] + 1j * kr[..., 1]
+
+    freqs = np.array([theta ** (-2.0 * j / dh) for j in range(dh // 2)])
+    # chunk 0 sits at positions 0..T-1: its stored keys are the un-rotated
+    # keys (RoPE at position 0 is the identity) turned by i * freq
+    g = {k: v.astype(np.float64) for k, v in w["global"].items()}
+    bw = {k: v.astype(np.float64) for k, v in w["blocks"][0].items()}
+    h0 = M.in_proj(g, st.noise(0).astype(np.float64))
+    _, k_plain, _ = M.block_qkv(cfg, bw, r.streams[0].mod[0, 0], h0, np.zeros(T, dtype=np.int64))
+    turn0 = np.exp(1j * np.arange(T)[:, None, None] * freqs[None, None, :])
+    np.testing.assert_allclose(as_complex(k0), as_complex(k_plain) * turn0, rtol=0, atol=1e-12)
+    for c in (1, 2):
+        kc = r.streams[0].kv[(0, 0, c)][0]
+        turn = np.exp(1j * c * T * freqs)[None, None, :]
+        np.testing.assert_allclose(as_complex(kc), as_complex(k0) * turn, rtol=0, atol=1e-12)

@@ -5,7 +5,8 @@ control loop that must not enter the CUDA allocator after start-up, or a
 framework that owns all device memory); its scratch is a fixed array inside
 the library.  Checked through the C ABI against psv_attention (caller
 scratch) on the same inputs, on two calls in a row (the second call reuses
-the array the first one left behind).  Kept in its own file, collected last.
+the array the first one left behind), with the call's status word read back
+after each.  Kept in its own file, collected last.
 """
 import numpy as np
 import pytest
@@ -31,8 +32,12 @@ def test_noalloc_matches_caller_scratch_on_two_calls():
         P.psv_attention_noalloc(prob, q.data_ptr(), k.data_ptr(), vt.data_ptr(), o.data_ptr(),
                                 torch.cuda.current_stream().cuda_stream)
 
+    stream = torch.cuda.current_stream().cuda_stream
     for _ in range(2):
         got = run_op(pb, call=noalloc)
+        # no device-side wait of the call gave up (the word is read from the
+        # library's own array, after the stream's work is done)
+        assert P.psv_attention_noalloc_status(stream) == 0
         T = pb["T"]
         for i in range(pb["n"]):
             assert rel_l2(got[i * T:(i + 1) * T], ref[i * T:(i + 1) * T]) <= 1e-2

@@ -31,6 +31,8 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "steady-state ms/chunk & chunks/s on 1 GB300; tensor-pipe % of BF16 peak"
+# every model configuration, measured after the headline one in the default run
+SWEEP = ["tiny", "wan21_1p3b", "wan22_5b", "wan21_1p3b_x8", "wan21_14b"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -63,6 +65,23 @@ def wave_bytes(cfg: dict) -> float:
     return weights + kv + latent
 
 
+def wave_roofline(cfg: dict, ms_wave: float, peaks: dict, peak_src: str) -> dict:
+    """Whole-wave roofline: max(FLOPs at the bf16 peak, bytes at the HBM copy
+    rate) against the measured wave time, for the burst and the sustained bf16
+    peaks (the timed region is a few hundred ms of back-to-back waves)."""
+    flops, bytes_ = wave_flops(cfg), wave_bytes(cfg)
+    hbm = peak_value(peaks, "hbm_gbs") * 1e9
+    out = {"flops_per_wave": flops, "bytes_per_wave": bytes_,
+           "tensor_tflops": flops / (ms_wave / 1e3) / 1e12, "peak_source": peak_src}
+    for tag, key in (("burst", "bf16_tflops"), ("sustained", "bf16_tflops_sustained")):
+        pk = peak_value(peaks, key) * 1e12
+        roof_ms = max(flops / pk, bytes_ / hbm) * 1e3
+        out[f"roofline_ms_{tag}"] = roof_ms
+        out[f"frac_{tag}"] = roof_ms / ms_wave
+    out["frac"] = out["frac_burst"]
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -84,8 +103,76 @@ def peak_value(peaks: dict, key: str):
     return FALLBACK_PEAKS[key]
 
 
-class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
+class NvmlClocks:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, by ctypes) every 20 ms in a thread during the timed region:
+    even a sub-second region gets many samples.  Read-only: no setting of
+    the GPU is changed."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.02):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        self.period = period_s
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        # the CUDA device's PCI address names the same GPU in NVML whatever
+        # CUDA_VISIBLE_DEVICES says; fall back to the index
+        found = False
+        try:
+            import torch
+
+            pr = torch.cuda.get_device_properties(index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            found = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) == 0
+        except Exception:
+            found = False
+        if not found and self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _one(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        self.samples.append((float(mhz.value), mw.value / 1000.0, int(rs.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._one()
+            self._stop.wait(self.period)
+
+    def start(self):
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        self._thread.join(timeout=5)
+        self._one()
+        sm = [x[0] for x in self.samples]
+        reasons = sorted({n for x in self.samples for bit, n in self.REASONS.items() if x[2] & bit})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": float(min(sm)),
+                "power_w_max": float(max(x[1] for x in self.samples)), "source": "nvml, 20 ms"}
+
+
+class SmiClocks:
+    """Fallback: nvidia-smi clock/throttle sampling (200 ms) during the timed region."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -133,7 +220,14 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 200 ms"}
+
+
+def ClockSampler(index: int):
+    try:
+        return NvmlClocks(index)
+    except Exception:
+        return SmiClocks(index)
 
 
 def dist_setup(args):
@@ -172,63 +266,82 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_wave_sample(cfg: dict, budget_s: float, min_blocks: int = 1):
-    """Time the f32 oracle on blocks of one steady wave (every task with a full
-    window, inputs drawn at the workload's shapes) until ``budget_s`` passed.
-    Returns (seconds per whole wave, blocks timed, threads)."""
-    from oracle import model as M
+class OracleWave:
+    """One steady wave of the f32 oracle at a configuration's shapes: every
+    task at a full window, its block inputs drawn once (seeded) at the
+    workload's sizes.  ``block()`` runs the oracle's transformer block for
+    every task of the wave once and returns the seconds it took."""
 
-    rng = np.random.default_rng(0)
-    d, T, W, S = cfg["d"], cfg["T"], cfg["W"], cfg["S"]
-    n_task = S * cfg["n_streams"]
-    specs = dict(synth.block_specs(cfg))
-    bw = {k: (rng.standard_normal(s, dtype=np.float32) * 0.02 if k.endswith("_w")
-              else np.zeros(s, np.float32)) for k, s in specs.items()}
-    tasks = []
-    for i in range(n_task):
-        c = W + (S - 1) - (i % S)
-        tasks.append(dict(
-            h=rng.standard_normal((T, d), dtype=np.float32),
-            mod=rng.standard_normal(6 * d, dtype=np.float32) * 0.1,
-            pos=M.positions(cfg, c),
-            window=[(rng.standard_normal((T, d), dtype=np.float32),
-                     rng.standard_normal((T, d), dtype=np.float32)) for _ in range(W)]))
-    t0 = time.perf_counter()
-    n_blocks = 0
-    while True:
-        for t in tasks:
-            M.block_forward(cfg, bw, t["mod"], t["h"], t["pos"], t["window"])
-        n_blocks += 1
-        el = time.perf_counter() - t0
-        if (el >= budget_s and n_blocks >= min_blocks) or n_blocks >= cfg["B"]:
-            break
-    per_block = el / n_blocks
-    threads = os.cpu_count() or 1
-    return per_block * cfg["B"], n_blocks, threads
+    def __init__(self, cfg: dict):
+        from oracle import model as M
+
+        self.M = M
+        self.cfg = cfg
+        rng = np.random.default_rng(0)
+        d, T, W, S = cfg["d"], cfg["T"], cfg["W"], cfg["S"]
+        self.n_task = S * cfg["n_streams"]
+        specs = dict(synth.block_specs(cfg))
+        self.bw = {k: (rng.standard_normal(s, dtype=np.float32) * 0.02 if k.endswith("_w")
+                       else np.zeros(s, np.float32)) for k, s in specs.items()}
+        self.tasks = []
+        for i in range(self.n_task):
+            c = W + (S - 1) - (i % S)
+            self.tasks.append(dict(
+                h=rng.standard_normal((T, d), dtype=np.float32),
+                mod=rng.standard_normal(6 * d, dtype=np.float32) * 0.1,
+                pos=M.positions(cfg, c),
+                window=[(rng.standard_normal((T, d), dtype=np.float32),
+                         rng.standard_normal((T, d), dtype=np.float32)) for _ in range(W)]))
+        self.threads = os.cpu_count() or 1
+
+    def block(self) -> float:
+        t0 = time.perf_counter()
+        for t in self.tasks:
+            self.M.block_forward(self.cfg, self.bw, t["mod"], t["h"], t["pos"], t["window"])
+        return time.perf_counter() - t0
+
+
+def oracle_wave_sample(cfg: dict, budget_s: float):
+    """Time the f32 oracle on blocks of one steady wave until ``budget_s``
+    passed (at least one block).  Returns (seconds per whole wave, blocks
+    timed, threads)."""
+    ow = OracleWave(cfg)
+    el, n = 0.0, 0
+    while n < cfg["B"] and (n == 0 or el < budget_s):
+        el += ow.block()
+        n += 1
+    return el / n * cfg["B"], n, ow.threads
 
 
 def run_reference(args, cfg_name, cfg, world, rank):
+    """The reference arm: the f32 oracle on the host cores.  One step is one
+    transformer block of a steady wave (all tasks at a full window); the
+    line's ms_per_step is the measured time of such a step, and the wave
+    (all B blocks) is extrapolated from it for ms_per_chunk and value."""
     if rank != 0:
         return 0
-    per_step = []
-    budget = max(0.5, args.ref_budget)
-    steps_total = args.warmup + args.steps
-    for i in range(steps_total):
-        wave_s, nb, threads = oracle_wave_sample(cfg, budget / steps_total, 1)
-        if i >= args.warmup:
-            per_step.append(wave_s)
-    wave_s = float(np.mean(per_step))
+    ow = OracleWave(cfg)
+    for _ in range(args.warmup):
+        ow.block()
+    per_step = [ow.block() for _ in range(args.steps)]
+    step_s = float(np.mean(per_step))
+    wave_s = step_s * cfg["B"]
     value = cfg["n_streams"] / wave_s
-    sample = (f"f32 numpy oracle, one transformer block of a steady {cfg['S'] * cfg['n_streams']}-task "
-              f"wave per step (all tasks at a full W={cfg['W']} window), scaled x{cfg['B']} blocks")
+    sample = (f"f32 numpy oracle: each step is one transformer block of a steady "
+              f"{ow.n_task}-task wave (all tasks at a full W={cfg['W']} window); "
+              f"ms_per_chunk and value extrapolate a step x{cfg['B']} blocks")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": wave_s * 1e3, "ms_per_chunk": wave_s * 1e3, "higher_is_better": True,
+        "ms_per_step": step_s * 1e3, "ms_per_chunk": wave_s * 1e3,
+        "step": "one transformer block of a steady wave (measured)",
+        "extrapolated": {"blocks_per_step": 1, "blocks_per_wave": cfg["B"],
+                         "ms_per_wave": wave_s * 1e3, "timed_s": float(np.sum(per_step))},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_name(cfg_name, cfg), "parallelism": "replicas",
                    "l2": "inputs larger than L2"},
-        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": ow.threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -365,16 +478,20 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
     tensor_kernel = name.startswith("gemm") or name == "attention"
     if tensor_kernel:
         achieved = t["flops"] / max(1, t["launches"]) / (per_launch_ms / 1e3) / 1e12
-        peak = peak_value(peaks, "bf16_tflops_sustained")
+        # the kernel is timed per launch (CUDA events around each launch of a
+        # short eager pass): the burst peak is its denominator
+        peak = peak_value(peaks, "bf16_tflops")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak}
+                "frac": achieved / peak,
+                "frac_of_sustained": achieved / peak_value(peaks, "bf16_tflops_sustained")}
     else:
         achieved = t["bytes"] / max(1, t["launches"]) / (per_launch_ms / 1e3) / 1e9
         peak = peak_value(peaks, "hbm_gbs")
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak}
     roof["kernel"] = name
-    roof["peak_source"] = f"{peak_src} ({'sustained bf16' if tensor_kernel else 'HBM copy'})"
+    roof["peak_source"] = f"{peak_src} ({'burst bf16' if tensor_kernel else 'HBM copy'})"
+    roof["ms_per_launch"] = per_launch_ms
     roof["traffic"] = None
     tfile = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if os.path.exists(tfile):
@@ -392,11 +509,7 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
                     roof["traffic"] = ent["bytes_per_launch"]
         except Exception:
             pass
-    flops = wave_flops(cfg)
-    bytes_ = wave_bytes(cfg)
-    bf16_peak = peak_value(peaks, "bf16_tflops_sustained") * 1e12
-    hbm_peak = peak_value(peaks, "hbm_gbs") * 1e9
-    roof_ms = max(flops / bf16_peak, bytes_ / hbm_peak) * 1e3
+    wave_roof = wave_roofline(cfg, ms_step, peaks, peak_src)
     kernels = {k: {"launches": v["launches"], "ms_per_launch": v["total_ms"] / max(1, v["launches"]),
                    "share": v["total_ms"] / max(1e-9, sum(x["total_ms"] for x in times.values()))}
                for k, v in times.items() if v["launches"]}
@@ -412,11 +525,7 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
                    "rows_per_wave": n_task * T, "parallelism": "replicas" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2 (bf16 weights + KV rings read every wave)",
                    "graphs": True},
-        "wave_roofline": {"flops_per_wave": flops, "bytes_per_wave": bytes_, "roofline_ms": roof_ms,
-                          "frac": roof_ms / ms_step,
-                          "tensor_tflops": flops / (ms_step / 1e3) / 1e12,
-                          "tensor_frac_of_bf16_peak": flops / (ms_step / 1e3) / bf16_peak,
-                          "peak_source": peak_src},
+        "wave_roofline": wave_roof,
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "chunks/s", "h2d_bytes_per_step": h2d,
@@ -427,8 +536,23 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
         "response_ms": S * ms_step,
     }
     sess.close()
+    del sess
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_sweep:
+        # every configuration's steady waves (the headline is the one above)
+        sweep = {}
+        for name in SWEEP:
+            if name == cfg_name:
+                sweep[name] = {"workload": workload_name(cfg_name, cfg), "steps": args.steps,
+                               "ms_per_chunk": ms_step, "chunks_per_s": n_st / (ms_step / 1e3),
+                               "wave_frac_burst": wave_roof["frac_burst"],
+                               "wave_frac_sustained": wave_roof["frac_sustained"],
+                               "tensor_tflops": wave_roof["tensor_tflops"], "headline": True}
+                continue
+            sweep[name] = measure_steady(name, local)
+        line["configs"] = sweep
     if rank == 0 and not args.no_cpu_baseline:
-        wave_s, nb, threads = oracle_wave_sample(cfg, args.ref_budget, 1)
+        wave_s, nb, threads = oracle_wave_sample(cfg, args.ref_budget)
         line["cpu_baseline"] = {
             "value": cfg["n_streams"] / wave_s, "unit": "chunks/s", "cores": threads,
             "kind": "oracle",
@@ -437,6 +561,71 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def measure_steady(cfg_name: str, local: int, min_seconds: float = 1.5, max_steps: int = 2000,
+                   warmup: int = 3) -> dict:
+    """ms/chunk of one configuration's steady waves (CUDA graphs, every task at
+    a full window), timed with CUDA events over at least ``min_seconds``; the
+    attention's time per launch from one eager profiled wave."""
+    import torch
+
+    from autoregressive_denoising_dit_gb300 import Session, _psv as P
+
+    cfg = synth.config(cfg_name)
+    S, W = cfg["S"], cfg["W"]
+    n_st = cfg["n_streams"]
+    fill = W + S - 1
+    peaks, peak_src = load_peaks()
+    est_ms = max(0.05, wave_flops(cfg) / (1.0e15) * 1e3)   # a first guess at 1 PFLOP/s
+    steps = int(min(max_steps, max(5, np.ceil(min_seconds * 1e3 / est_ms))))
+    n_resident = fill + warmup + 2 * steps + 2
+    sess = Session(cfg, max_streams=n_st, max_inflight=n_resident + S + 8)
+    try:
+        sess.load_device_weights(synth.iter_device_weights(cfg, seed=0, device=f"cuda:{local}"))
+        torch.cuda.synchronize()
+        streams = synth.make_streams(cfg)
+        sids = [sess.open_stream(st.cond) for st in streams]
+        rng = np.random.default_rng(7)
+        for c in range(n_resident):
+            for sid in sids:
+                sess.submit(sid, rng.standard_normal((cfg["T"], cfg["C"]), dtype=np.float32))
+        for _ in range(fill + warmup):
+            sess.run_wave()
+        sess.sync(600000)
+        stream = sess.torch_stream
+        # one timed probe wave sets the step count for the time target
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sess.run_wave()
+        b.record(stream)
+        torch.cuda.synchronize()
+        steps = int(min(max_steps, max(5, np.ceil(min_seconds / max(1e-6, a.elapsed_time(b) / 1e3)))))
+        steps = min(steps, n_resident - fill - warmup - 2)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            n = sess.run_wave()
+            assert n == S * n_st, f"{cfg_name}: wave is not steady ({n} tasks)"
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        P.psv_set_profiling(sess.ctx, True)
+        sess.run_wave()
+        times = P.psv_kernel_times(sess.ctx)
+        P.psv_set_profiling(sess.ctx, False)
+        sess.sync(600000)
+    finally:
+        sess.close()
+        torch.cuda.empty_cache()
+    at = times.get("attention", {})
+    att_us = at.get("total_ms", 0.0) / max(1, at.get("launches", 0)) * 1e3 if at else None
+    att_tf = (at["flops"] / at["launches"] / (att_us / 1e6) / 1e12) if at and att_us else None
+    roof = wave_roofline(cfg, ms, peaks, peak_src)
+    return {"workload": workload_name(cfg_name, cfg), "steps": steps, "ms_per_chunk": ms,
+            "chunks_per_s": n_st / (ms / 1e3), "wave_frac_burst": roof["frac_burst"],
+            "wave_frac_sustained": roof["frac_sustained"], "tensor_tflops": roof["tensor_tflops"],
+            "attention_us_per_launch": att_us, "attention_tflops": att_tf}
 
 
 def run_latency(args, cfg_name, cfg, world, rank, local):
@@ -536,6 +725,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=15.0,
                     help="seconds of CPU time for the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the steady-wave timing of the other model configurations")
     ap.add_argument("--latency-mode", action="store_true",
                     help="time the latency-mode schedule (each stream's oldest chunk per wave)")
     ap.add_argument("--blocks", type=int, default=None,

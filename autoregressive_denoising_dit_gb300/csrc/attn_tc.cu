@@ -24,10 +24,12 @@
 //                on the even CTA also the reader of the work queue
 //   warp 1       TMEM allocator (both CTAs) and MMA issuer (even CTA)
 //   warp 2       TMA: this CTA's V^T halves (3 stages)
-//   warps 4..11  softmax, two threads per query row, 128 keys each of a
-//                256-key tile (the row max is exchanged through shared
-//                memory); online max/sum in the log2 domain with lazy O
-//                rescale (only when the running max grows by more than 2^8)
+//   warps 4..11  softmax, two threads per query row in one warp (lanes l
+//                and l + 16), 128 keys each of a 256-key tile, through
+//                16-lane TMEM accesses: the row max and sum need one
+//                shuffle, no shared memory and no barrier; online max/sum in
+//                the log2 domain with lazy O rescale (only when the running
+//                max grows by more than 2^8)
 // The first warpgroup hands registers to the two softmax warpgroups
 // (setmaxnreg), so that a softmax thread holds its 128 scores without
 // spilling: local-memory traffic would compete with the MMAs' shared-memory
@@ -89,11 +91,9 @@ struct AttnCfg {
   static constexpr int N_BARS = 12 + 4 * kStages;
   // barriers, the TMEM address word and the merge flag, two published piece
   // slots and the softmax warps' copy (two int4 each: the piece and its task
-  // fields), then the row-max /
-  // row-sum exchange area [2 key halves][128 rows] f32.  The dynamic
-  // shared-memory window starts 1024-byte aligned (no static shared
-  // variables; checked at run time).
-  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 6 * 16 + 2 * QT * 4;
+  // fields).  The dynamic shared-memory window starts 1024-byte aligned (no
+  // static shared variables; checked at run time).
+  static constexpr size_t SMEM = OFF_BAR + N_BARS * 8 + 16 + 6 * 16;
   static constexpr int OH = DH / 2;              // O columns per thread
   static constexpr int OC = OH < 32 ? OH : 32;   // O columns per TMEM access
   static_assert(V_ATOM % 1024 == 0 && K_ATOM % 1024 == 0, "swizzle atoms stay 1024-aligned");
@@ -120,45 +120,88 @@ __device__ __forceinline__ void umma_pair_tmem_a(uint32_t tmem_d, uint32_t tmem_
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+// 16-lane accesses of TMEM (shape 16x32bx2): threads 0-15 of the warp reach
+// lanes [base, base + 16) at column c, threads 16-31 the same lanes at column
+// c + SPLIT.  This lets the two threads of a query row that hold the two
+// halves of its keys (or of its O columns) sit in one warp, so the row's max
+// and sum are combined with one shuffle.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, float* v) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr), "n"(SPLIT));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float* v) {
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+      : "r"(taddr), "n"(SPLIT));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// O-column access of OC (16 or 32) f32 columns.
-template <int OC>
-__device__ __forceinline__ void o_ld(uint32_t taddr, float* v) {
-  if constexpr (OC == 32) tmem_ld32(taddr, v);
-  else tmem_ld16f(taddr, v);
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st16x2_16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, "
+      "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(taddr),
+      "n"(SPLIT), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+      "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+      "r"(v[14]), "r"(v[15])
+      : "memory");
 }
-template <int OC>
-__device__ __forceinline__ void o_st(uint32_t taddr, const float* v) {
-  if constexpr (OC == 32) {
-    tmem_st32(taddr, v);
-  } else {
-    uint32_t u[16];
+
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st16x2_32f(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, "
+      "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};" ::"r"(taddr),
+      "n"(SPLIT), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+      "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+      "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// O-column access of OC (16 or 32) f32 columns of this thread's half of its
+// row's O: columns [c, c + OC) for threads 0-15, [c + OH, c + OH + OC) for
+// threads 16-31.
+template <int OC, int OH>
+__device__ __forceinline__ void o_ld(uint32_t taddr, float* v) {
+  if constexpr (OC == 32) tmem_ld16x2_32<OH>(taddr, v);
+  else tmem_ld16x2_16<OH>(taddr, v);
+}
+template <int OH>
+__device__ __forceinline__ void o_st16(uint32_t taddr, const float* v) {
+  uint32_t u[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
-    tmem_st16(taddr, u);
-  }
+  for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
+  tmem_st16x2_16<OH>(taddr, u);
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -357,7 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_last_p = reinterpret_cast<int*>(tmem_slot + 1);
   int4* pc_slot = reinterpret_cast<int4*>(tmem_slot + 4);   // [2][2] published pieces
   int4* sm_piece = pc_slot + 4;                             // [2] the softmax warps' copy
-  float* xch = reinterpret_cast<float*>(sm_piece + 2);      // [2 key halves][128 rows]
 
   pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
@@ -576,14 +618,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    // ---------------- softmax: two threads per query row r of this CTA
-    const int hk = (warp - 4) >> 2;  // key half of the tile: keys [128 hk, 128 hk + 128)
-    const int q = warp & 3;          // TMEM lane quadrant the warp may access
-    const int r = q * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t s_addr = tmem + COL_S + hk * 128 + lane_off;
-    const uint32_t p_addr = tmem + COL_P + hk * 64 + lane_off;
-    const uint32_t o_addr = tmem + COL_O + hk * Cfg::OH + lane_off;
+    // ---------------- softmax: two threads per query row r of this CTA, in
+    // one warp: lanes l and l + 16 hold keys [0, 128) and [128, 256) of a
+    // tile of the same row (16-lane TMEM accesses), so the row max and sum
+    // are one shuffle away.  Warp 4 + 4h + q serves rows 32 q + 16 h + [0, 16)
+    // (q: the TMEM lane quadrant the warp may access).
+    const int hk = lane >> 4;         // key half of the tile: keys [128 hk, 128 hk + 128)
+    const int q = warp & 3;
+    const int rb = q * 32 + ((warp - 4) >> 2) * 16;  // first row of the warp
+    const int r = rb + (lane & 15);
+    const uint32_t lane_off = static_cast<uint32_t>(rb) << 16;
+    const uint32_t s_addr = tmem + COL_S + lane_off;
+    const uint32_t p_addr = tmem + COL_P + lane_off;
+    const uint32_t o_addr = tmem + COL_O + lane_off;
     const uint32_t s_free0 = mapa_shared(s_free, 0);
     const uint32_t p_full_a0 = mapa_shared(p_full_a, 0);
     const uint32_t p_full_b0 = mapa_shared(p_full_b, 0);
@@ -618,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, s + c * 32);
+          for (int c = 0; c < 4; ++c) tmem_ld16x2_32<128>(s_addr + c * 32, s + c * 32);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
@@ -641,11 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx_half = fmaxf(max3(mx8[0], mx8[1], mx8[2]),
                           fmaxf(max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         }
-        // Row max over both key halves (shared-memory exchange).
-        xch[hk * QT + r] = mx_half;
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        const float other_mx = xch[(1 - hk) * QT + r];
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // Row max over both key halves: the other half is in lane l ^ 16.
+        const float other_mx = __shfl_xor_sync(0xffffffffu, mx_half, 16);
         if (!ok) continue;
         const float m_tile = fmaxf(mx_half, other_mx) * sl2;
         const bool grow = m_tile > m + kRescaleThreshold;
@@ -683,23 +727,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < Cfg::OH / 16; ++c) {
             float o[16];
-            tmem_ld16f(o_addr + c * 16, o);
+            tmem_ld16x2_16<Cfg::OH>(o_addr + c * 16, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] *= alpha;
-            o_st<16>(o_addr + c * 16, o);
+            o_st16<Cfg::OH>(o_addr + c * 16, o);
           }
         }
-        tmem_st16(p_addr, pk0);
-        tmem_st16(p_addr + 16, pk1);
+        tmem_st16x2_16<64>(p_addr, pk0);
+        tmem_st16x2_16<64>(p_addr + 16, pk1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(p_full_a0);
         exp_chunk(2, pk0);
-        tmem_st16(p_addr + 32, pk0);
+        tmem_st16x2_16<64>(p_addr + 32, pk0);
         exp_chunk(3, pk1);
-        tmem_st16(p_addr + 48, pk1);
+        tmem_st16x2_16<64>(p_addr + 48, pk1);
         l = l * alpha + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
         tmem_wait_st();
         tc_fence_before();
@@ -710,9 +754,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
       g += nT;
       // Row sum over both key halves, fixed order (half 0 + half 1).
-      xch[hk * QT + r] = l;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      l = xch[r] + xch[QT + r];
+      {
+        const float lo = __shfl_xor_sync(0xffffffffu, l, 16);
+        l = hk == 0 ? l + lo : lo + l;
+      }
       // O is read (below) before this thread writes any P of the next piece,
       // whose first P.V overwrites it.
       const int qloc0 = pg.unit * 2 * QT + rank * QT;  // first query row of this CTA within the task
@@ -741,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
             float o[Cfg::OC];
-            o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
+            o_ld<Cfg::OC, Cfg::OH>(o_addr + c * Cfg::OC, o);
             tmem_wait_ld();
             if (valid) store_row(o, c, inv_l);
           }
@@ -758,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < Cfg::OH / Cfg::OC; ++c) {
             float o[Cfg::OC];
-            o_ld<Cfg::OC>(o_addr + c * Cfg::OC, o);
+            o_ld<Cfg::OC, Cfg::OH>(o_addr + c * Cfg::OC, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < Cfg::OC; ++e) mine[(hk * Cfg::OH + c * Cfg::OC + e) * QT + r] = o[e];

@@ -467,9 +467,12 @@ psv::GemmParams base_gemm(const psv_ctx* ctx, int M) {
   return p;
 }
 
+// CTAs of a GEMM launch: two per 256-row pair tile (the two CTAs of a pair
+// take the two 128-row halves), at most one per SM.
 int gemm_grid(const psv_ctx* ctx, int M, int N) {
-  const int tiles = ((M + psv::kGemmBM - 1) / psv::kGemmBM) * ((N + psv::kGemmBN - 1) / psv::kGemmBN);
-  return std::max(1, std::min(tiles, ctx->sm_count));
+  const int m_pairs = ((M + psv::kGemmBM - 1) / psv::kGemmBM + 1) / 2;
+  const int tiles = m_pairs * ((N + psv::kGemmBN - 1) / psv::kGemmBN);
+  return std::max(2, std::min(2 * tiles, ctx->sm_count));
 }
 
 // Enqueue every kernel of one wave of n tasks (task table already on the
@@ -822,7 +825,7 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
     {
       uint64_t dims[3] = {d, static_cast<uint64_t>(L.Lr), static_cast<uint64_t>(L.n_rings)};
       uint64_t str[2] = {d * 2, d * 2 * L.Lr};
-      uint32_t box[3] = {aw, 128, 1};
+      uint32_t box[3] = {aw, psv::attn_k_box_rows(), 1};
       ok &= encode_bf16(&ctx->tmK, 3, ctx->arena + L.k_ring, dims, str, box, swq);
       if (d % 64 == 0) {
         uint32_t obox[3] = {64, 32, 1};

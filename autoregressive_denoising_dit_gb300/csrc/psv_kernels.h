@@ -94,8 +94,8 @@ struct AttnParams {
 constexpr int kAttnSplitMinTiles = 64;
 // Tail units (the last query unit of a task when its rows fit in one CTA,
 // e.g. 24 of T = 1560) cost as much as a full unit; from this many key tiles
-// they are split into two halves, which the work queue hands out last so that
-// they fill the end of the launch.
+// (2K keys) they are split into two halves, short pieces that the work queue
+// hands out late so that they even out the end of the launch.
 constexpr int kAttnTailSplitMinTiles = 8;
 constexpr int kQueueInts = 2;
 // Query units of 256 rows per (task, head).
@@ -112,6 +112,9 @@ size_t attn_counter_ints(int max_tasks, int T, int H);
 // Each CTA of a pair loads dh/2 rows of a V^T tile: the box height of the
 // V^T tensor map.
 inline uint32_t attn_v_box_rows(int dh) { return static_cast<uint32_t>(dh / 2); }
+// Each CTA of a pair loads 128 keys of a 256-key tile: the box height of the
+// K tensor map.
+inline uint32_t attn_k_box_rows() { return 128u; }
 
 constexpr int kGemmBM = 128, kGemmBN = 256;  // rows per CTA, columns of the narrow pair tile
 size_t gemm_smem_bytes();

@@ -70,7 +70,7 @@ int psv_attention_enqueue(const psv_attn_problem* p, const void* q, const void* 
     uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(p->k_rows),
                         static_cast<uint64_t>(p->n)};
     uint64_t str[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(d) * 2 * p->k_rows};
-    uint32_t box[3] = {aw, 128, 1};
+    uint32_t box[3] = {aw, psv::attn_k_box_rows(), 1};
     ok &= psv::encode_bf16_map(&tmK, 3, const_cast<void*>(k), dims, str, box, swq);
   }
   {

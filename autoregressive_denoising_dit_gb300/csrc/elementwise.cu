@@ -138,21 +138,53 @@ __global__ void __launch_bounds__(IP_THREADS)
   for (int i = 0; i < IP_RG; ++i)
 #pragma unroll
     for (int j = 0; j < IP_CG; ++j) acc[i][j] = 0.0f;
+  // 16-byte loads of x (4 floats) and W (8 bf16) when C allows them
+  const bool vec = (C % 8) == 0;
   for (int k0 = 0; k0 < C; k0 += IP_KC) {
-    for (int idx = threadIdx.x; idx < IP_ROWS * IP_KC; idx += IP_THREADS) {
-      const int rr = idx / IP_KC, kk = idx % IP_KC;
-      const int row = r0 + rr, k = k0 + kk;
-      float xv = 0.0f;
-      if (row < M && k < C) {
-        const TaskDev& t = tasks[row / T];
-        xv = state[(static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k];
+    if (vec) {
+      for (int idx = threadIdx.x; idx < IP_ROWS * (IP_KC / 4); idx += IP_THREADS) {
+        const int rr = idx / (IP_KC / 4), kq = idx % (IP_KC / 4);
+        const int row = r0 + rr, k = k0 + kq * 4;
+        float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < M && k < C) {
+          const TaskDev& t = tasks[row / T];
+          xv = *reinterpret_cast<const float4*>(
+              state + (static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k);
+        }
+        xs[rr][kq * 4] = xv.x;
+        xs[rr][kq * 4 + 1] = xv.y;
+        xs[rr][kq * 4 + 2] = xv.z;
+        xs[rr][kq * 4 + 3] = xv.w;
       }
-      xs[rr][kk] = xv;
-    }
-    for (int idx = threadIdx.x; idx < IP_KC * IP_COLS; idx += IP_THREADS) {
-      const int nn = idx / IP_KC, kk = idx % IP_KC;  // k fastest: coalesced weight rows
-      const int col = c0 + nn, k = k0 + kk;
-      ws[kk][nn] = (col < d && k < C) ? __bfloat162float(w_in[static_cast<int64_t>(col) * C + k]) : 0.0f;
+      for (int idx = threadIdx.x; idx < IP_COLS * (IP_KC / 8); idx += IP_THREADS) {
+        const int nn = idx / (IP_KC / 8), kq = idx % (IP_KC / 8);
+        const int col = c0 + nn, k = k0 + kq * 8;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (col < d && k < C) raw = *reinterpret_cast<const uint4*>(w_in + static_cast<int64_t>(col) * C + k);
+        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(w2[e]);
+          ws[kq * 8 + 2 * e][nn] = f.x;
+          ws[kq * 8 + 2 * e + 1][nn] = f.y;
+        }
+      }
+    } else {
+      for (int idx = threadIdx.x; idx < IP_ROWS * IP_KC; idx += IP_THREADS) {
+        const int rr = idx / IP_KC, kk = idx % IP_KC;
+        const int row = r0 + rr, k = k0 + kk;
+        float xv = 0.0f;
+        if (row < M && k < C) {
+          const TaskDev& t = tasks[row / T];
+          xv = state[(static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k];
+        }
+        xs[rr][kk] = xv;
+      }
+      for (int idx = threadIdx.x; idx < IP_KC * IP_COLS; idx += IP_THREADS) {
+        const int nn = idx / IP_KC, kk = idx % IP_KC;  // k fastest: coalesced weight rows
+        const int col = c0 + nn, k = k0 + kk;
+        ws[kk][nn] = (col < d && k < C) ? __bfloat162float(w_in[static_cast<int64_t>(col) * C + k]) : 0.0f;
+      }
     }
     __syncthreads();
 #pragma unroll 4

@@ -261,6 +261,49 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+// V^T of one warp's 32 rows x 64 columns [n0, n0 + 64) of the v section:
+// per 32 columns (one head, dims e0..e0+31) a [32 dims][32 tokens] bf16 box,
+// transposed through the warp's staging buffer and written by one TMA store
+// into the task's ring rows of the transposed V ring (tme: [rings*H][dh][Lp],
+// 32 x 32 boxes, no swizzle).  The caller checks that the warp's rows lie in
+// one task and below M, and that ring rows start 8-aligned (T % 8 == 0).
+__device__ __forceinline__ void vt_chunk64(const GemmParams& p, const CUtensorMap* tme, void* stage,
+                                           int row0, int n0, float* v) {
+  const int lane = lane_id();
+  const TaskDev& t = p.tasks[row0 / p.T];
+  const int rr0 = t.slot * p.T + (row0 - t.row0);  // first ring row of the warp's tokens
+  const int ring = t.ring0 + p.block * p.S;
+  uint16_t* st16 = reinterpret_cast<uint16_t*>(stage);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = n0 + 32 * h - 2 * p.d;
+    const int head = j / p.dh, e0 = j - head * p.dh;
+    const float4* b4 = reinterpret_cast<const float4*>(p.bias + n0 + 32 * h);
+    float* vh = v + 32 * h;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 bb = __ldg(b4 + i);
+      vh[4 * i] += bb.x;
+      vh[4 * i + 1] += bb.y;
+      vh[4 * i + 2] += bb.z;
+      vh[4 * i + 3] += bb.w;
+    }
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(vh[i]);
+      st16[i * 32 + lane] = *reinterpret_cast<const uint16_t*>(&b);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tme, stage, rr0, e0, ring * p.H + head);
+      bulk_commit();
+    }
+  }
+}
+
 // QKV epilogue of one warp's 32 rows x 64 columns [n0, n0 + 64).  q and k
 // (bias, RoPE) are staged as a 128-byte-swizzled [32][64] bf16 box and
 // written by one TMA store: q into [rows][d] (tmq), k into the task's ring
@@ -269,11 +312,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 // (a box must not reach into the next task's ring rows); the few warps that
 // straddle a task boundary, and V^T (stored transposed), go row by row.
 __device__ __forceinline__ void qkv_chunk64(const GemmParams& p, const CUtensorMap* tmq,
-                                            const CUtensorMap* tmk, void* stage, int row, int row0,
-                                            int n0, float* v) {
+                                            const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                            void* stage, int row, int row0, int n0, float* v) {
   if (n0 >= p.N) return;
   const int sec = n0 / p.d;
   const int last = row0 + 31;
+  if (sec == 2 && p.vt_box && (p.dh % 32) == 0 && last < p.M && row0 / p.T == last / p.T) {
+    vt_chunk64(p, tmv, stage, row0, n0, v);
+    return;
+  }
   const bool box = (p.d % 64) == 0 && sec < 2 && last < p.M && row0 / p.T == last / p.T;
   if (!box) {
     epilogue32<EPI_QKV>(p, row, n0, v);
@@ -333,7 +380,8 @@ __global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC,
-                   const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ CUtensorMap tmE, const GemmParams p) {
   using G = GemmShape<WIDE>;
   constexpr int BN = G::BN, BK = G::BK, STAGES = G::STAGES, KA = G::KA;
   constexpr int A_ATOM = G::A_ATOM, B_ATOM = G::B_ATOM, A_BYTES = G::A_BYTES, B_BYTES = G::B_BYTES;
@@ -486,7 +534,7 @@ __global__ void __launch_bounds__(320, 1)
           if constexpr (EPI == EPI_GELU)
             gelu_chunk64(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
           else
-            qkv_chunk64(p, &tmC, &tmD, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+            qkv_chunk64(p, &tmC, &tmD, &tmE, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
         }
       } else {
 #pragma unroll 1
@@ -524,7 +572,8 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int EPI, bool WIDE>
 cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
-                       const CUtensorMap* tmD, const GemmParams& p, int max_ctas, cudaStream_t st) {
+                       const CUtensorMap* tmD, const CUtensorMap* tmE, const GemmParams& p,
+                       int max_ctas, cudaStream_t st) {
   static uint64_t set_up = 0;
   static int max_clusters_dev[64] = {};
   const size_t smem = GemmShape<WIDE>::SMEM;
@@ -564,7 +613,7 @@ cudaError_t launch_one(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUt
   if (max_ctas >= 2 && clusters > max_ctas / 2) clusters = max_ctas / 2;
   cfg.gridDim = dim3(2 * clusters);
   cfg.numAttrs = 2;  // + programmatic stream serialization
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, WIDE>, *tmA, *tmB, *tmC, *tmD, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, WIDE>, *tmA, *tmB, *tmC, *tmD, *tmE, p);
 }
 
 }  // namespace
@@ -579,24 +628,26 @@ size_t gemm_smem_bytes() {
 bool use_wide(int epi, int K) { return epi == EPI_RESID && K >= 4096; }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmC, const CUtensorMap* tmD, const GemmParams& p,
-                        int grid, cudaStream_t st) {
+                        const CUtensorMap* tmC, const CUtensorMap* tmD, const CUtensorMap* tmE,
+                        const GemmParams& p, int grid, cudaStream_t st) {
   if ((epi == EPI_RESID || epi == EPI_GELU) && !tmC) return cudaErrorInvalidValue;
   if (epi == EPI_QKV && p.d % 64 == 0 && (!tmC || !tmD)) return cudaErrorInvalidValue;
+  if (epi == EPI_QKV && p.vt_box && !tmE) return cudaErrorInvalidValue;
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
   const CUtensorMap* dm = tmD ? tmD : tmA;
+  const CUtensorMap* em = tmE ? tmE : tmA;
   const bool wide = use_wide(epi, p.K);
   switch (epi) {
     case EPI_QKV:
-      return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, dm, p, grid, st)
-                  : launch_one<EPI_QKV, false>(tmA, tmB, c, dm, p, grid, st);
+      return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, dm, em, p, grid, st)
+                  : launch_one<EPI_QKV, false>(tmA, tmB, c, dm, em, p, grid, st);
     case EPI_RESID:
-      return wide ? launch_one<EPI_RESID, true>(tmA, tmB, c, dm, p, grid, st)
-                  : launch_one<EPI_RESID, false>(tmA, tmB, c, dm, p, grid, st);
+      return wide ? launch_one<EPI_RESID, true>(tmA, tmB, c, dm, em, p, grid, st)
+                  : launch_one<EPI_RESID, false>(tmA, tmB, c, dm, em, p, grid, st);
     case EPI_GELU:
-      return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, dm, p, grid, st)
-                  : launch_one<EPI_GELU, false>(tmA, tmB, c, dm, p, grid, st);
-    case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, dm, p, grid, st);
+      return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, dm, em, p, grid, st)
+                  : launch_one<EPI_GELU, false>(tmA, tmB, c, dm, em, p, grid, st);
+    case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, dm, em, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -296,6 +296,8 @@ struct psv_ctx {
   CUtensorMap tmC_u;  // bf16 u, written by the GELU epilogue's TMA stores
   CUtensorMap tmC_q;  // bf16 q and the K ring, written by the QKV epilogue's
   CUtensorMap tmC_k;  // TMA stores (32-row x 64-column boxes)
+  CUtensorMap tmC_vt;  // the transposed V ring, 32 x 32 boxes (QKV epilogue)
+  bool vt_box = false;
   // executor
   bool use_graphs = true;
   std::map<int64_t, int> shape_seen;
@@ -523,8 +525,10 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.vt_ring = ctx->at<__nv_bfloat16>(L.vt_ring);
       p.rope_local = ctx->at<float2>(L.rope_local);
       p.rope_base = ctx->at<float2>(L.rope_base);
+      p.vt_box = ctx->vt_box ? 1 : 0;
       run.run(K_GEMM_QKV, 2.0 * Md * 3 * d, Md * 2 + 3.0 * d * d * 2 + 3 * Md * 2, [&] {
-        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, &ctx->tmC_q, &ctx->tmC_k, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_QKV, &ctx->tmA_y, &ctx->tmB_qkv, &ctx->tmC_q, &ctx->tmC_k,
+                                ctx->vt_box ? &ctx->tmC_vt : nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // window attention
@@ -563,7 +567,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 2 * d;
       run.run(K_GEMM_O, 2.0 * Md * d, Md * 2 + 1.0 * d * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, &ctx->tmC_h, nullptr, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_o, &ctx->tmB_o, &ctx->tmC_h, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // LN2 + modulation
@@ -581,7 +585,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.bias = ctx->at<float>(L.b_up) + static_cast<size_t>(b) * F;
       p.u = ctx->at<__nv_bfloat16>(L.u);
       run.run(K_GEMM_UP, 2.0 * Md * F, Md * 2 + 1.0 * F * d * 2 + static_cast<double>(M) * F * 2, [&] {
-        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, &ctx->tmC_u, nullptr, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_GELU, &ctx->tmA_y, &ctx->tmB_up, &ctx->tmC_u, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     // down + gated residual (gate2)
@@ -596,7 +600,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
       p.mod = ctx->at<float>(L.mod);
       p.gate_off = 5 * d;
       run.run(K_GEMM_DOWN, 2.0 * Md * F, static_cast<double>(M) * F * 2 + 1.0 * F * d * 2 + Md * 8, [&] {
-        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, &ctx->tmC_h, nullptr, p, gemm_grid(ctx, M, p.N), st);
+        return psv::launch_gemm(psv::EPI_RESID, &ctx->tmA_u, &ctx->tmB_down, &ctx->tmC_h, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
       });
     }
     if (tap && b == ctx->tap_block && run.err == cudaSuccess)
@@ -616,7 +620,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     p.bias = ctx->at<float>(L.b_out);
     p.state = ctx->at<float>(L.state);
     run.run(K_GEMM_FINAL, 2.0 * Md * m.C, Md * 2 + static_cast<double>(M) * m.C * 8, [&] {
-      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
+      return psv::launch_gemm(psv::EPI_EULER, &ctx->tmA_y, &ctx->tmB_out, nullptr, nullptr, nullptr, p, gemm_grid(ctx, M, p.N), st);
     });
   }
   return run.err;
@@ -841,6 +845,14 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       uint64_t str[2] = {static_cast<uint64_t>(L.Lp) * 2, static_cast<uint64_t>(L.Lp) * 2 * m.dh};
       uint32_t box[3] = {64, psv::attn_v_box_rows(m.dh), 1};
       ok &= encode_bf16(&ctx->tmV, 3, ctx->arena + L.vt_ring, dims, str, box, SW128);
+      // V^T boxes of 32 tokens x 32 dims, stored by the QKV epilogue: their
+      // first token (a ring row) must be 8-aligned, so T % 8 == 0
+      ctx->vt_box = m.T % 8 == 0 && m.dh % 32 == 0;
+      if (ctx->vt_box) {
+        uint32_t vbox[3] = {32, 32, 1};
+        ok &= encode_bf16(&ctx->tmC_vt, 3, ctx->arena + L.vt_ring, dims, str, vbox,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+      }
     }
     if (!ok) {
       set_err(ctx, PSV_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");

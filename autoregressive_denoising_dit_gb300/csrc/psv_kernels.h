@@ -54,6 +54,7 @@ struct GemmParams {
   __nv_bfloat16* k_ring;   // [rings][Lr][d]
   __nv_bfloat16* vt_ring;  // [rings][H][dh][Lp]
   int Lr, Lp;
+  int vt_box;              // 1: V^T through TMA stores of 32 x 32 boxes (tmE)
   const float2* rope_local;  // [dh/2][T]   (cos, sin) of i * f_j
   const float2* rope_base;   // [slots][dh/2] (cos, sin) of c*T * f_j
   // EPI_RESID
@@ -124,11 +125,12 @@ size_t attn_smem_bytes(int dh);
 // box 32 x 32, 128-byte swizzle) for EPI_RESID (TMA reduce-add), bf16 u
 // ([rows][F], box 64 x 32, 128-byte swizzle) for EPI_GELU, bf16 q ([rows][d],
 // box 64 x 32, 128-byte swizzle) for EPI_QKV; tmD: bf16 K ring ([rings][Lr][d],
-// box 64 x 32 x 1, 128-byte swizzle) for EPI_QKV (both needed when d % 64 == 0).
-// The others ignore them.
+// box 64 x 32 x 1, 128-byte swizzle) for EPI_QKV (both needed when d % 64 == 0);
+// tmE: bf16 V^T ring ([rings*H][dh][Lp], box 32 x 32 x 1, no swizzle) for
+// EPI_QKV when p.vt_box is set.  The others ignore them.
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                        const CUtensorMap* tmC, const CUtensorMap* tmD, const GemmParams& p,
-                        int grid, cudaStream_t st);
+                        const CUtensorMap* tmC, const CUtensorMap* tmD, const CUtensorMap* tmE,
+                        const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, const AttnParams& p, int n_tasks, int grid,
                              cudaStream_t st);

@@ -115,6 +115,101 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
+// The same LayerNorm for wide rows (d > 2048): ROWW warps share a row, each
+// holding up to MAXV float4 per lane (interleaved, so every warp load is 512
+// contiguous bytes), and the row's partial sums meet in shared memory in a
+// fixed order (deterministic).  One warp per row would need 40 float4 per lane
+// at d = 5120, which leaves one CTA per SM.
+template <int MAXV, int ROWW>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_mod_wide_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int M, int d,
+                       int T, const TaskDev* __restrict__ tasks, const float* __restrict__ table,
+                       int use_fmod, int block, int shift_off, int scale_off, float eps) {
+  extern __shared__ float4 ln_smem[];  // [2][d / 4]: shift, scale
+  __shared__ float red[2][LN_WARPS];
+  constexpr int RPC = LN_WARPS / ROWW;  // rows per CTA
+  pdl_trigger();
+  pdl_wait();  // h is the previous kernel's output
+  const int warp = warp_id(), lane = lane_id();
+  const int row0 = blockIdx.x * RPC;
+  const int row = row0 + warp / ROWW;
+  const int part = warp % ROWW;
+  const int nv = d >> 2;
+  auto mod_base = [&](int r) {
+    const TaskDev& t = tasks[r / T];
+    return table + (use_fmod ? static_cast<int64_t>(t.fmod0)
+                             : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
+  };
+  float4 v[MAXV];
+  float s = 0.0f;
+  if (row < M) {
+    const float4* hr = reinterpret_cast<const float4*>(h + static_cast<int64_t>(row) * d);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int k = part * 32 + lane + i * 32 * ROWW;
+      if (k < nv) {
+        v[i] = __ldcs(hr + k);
+        s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
+    }
+  }
+  {
+    const float* base = mod_base(row0);
+    const float4* shift = reinterpret_cast<const float4*>(base + shift_off);
+    const float4* scale = reinterpret_cast<const float4*>(base + scale_off);
+    for (int k = threadIdx.x; k < nv; k += LN_WARPS * 32) {
+      ln_smem[k] = __ldg(shift + k);
+      ln_smem[nv + k] = __ldg(scale + k);
+    }
+  }
+  s = warp_sum(s);
+  if (lane == 0) red[0][warp] = s;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < ROWW; ++w) tot += red[0][(warp / ROWW) * ROWW + w];
+  const float mean = tot / static_cast<float>(d);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = part * 32 + lane + i * 32 * ROWW;
+    if (row < M && k < nv) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+      q += (a * a + b * b) + (c * c + e * e);
+    }
+  }
+  q = warp_sum(q);
+  if (lane == 0) red[1][warp] = q;
+  __syncthreads();
+  if (row >= M) return;
+  float qt = 0.0f;
+#pragma unroll
+  for (int w = 0; w < ROWW; ++w) qt += red[1][(warp / ROWW) * ROWW + w];
+  const float rstd = rsqrtf(qt / static_cast<float>(d) + eps);
+  const bool own_task = (row / T) == (row0 / T);
+  const float4* shift = ln_smem;
+  const float4* scale = ln_smem + nv;
+  if (!own_task) {
+    const float* base = mod_base(row);
+    shift = reinterpret_cast<const float4*>(base + shift_off);
+    scale = reinterpret_cast<const float4*>(base + scale_off);
+  }
+  uint2* yr = reinterpret_cast<uint2*>(y + static_cast<int64_t>(row) * d);
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int k = part * 32 + lane + i * 32 * ROWW;
+    if (k < nv) {
+      const float4 sh = shift[k], sc = scale[k];
+      uint2 o;
+      o.x = pack_bf16x2((v[i].x - mean) * rstd * (1.0f + sc.x) + sh.x,
+                        (v[i].y - mean) * rstd * (1.0f + sc.y) + sh.y);
+      o.y = pack_bf16x2((v[i].z - mean) * rstd * (1.0f + sc.z) + sh.z,
+                        (v[i].w - mean) * rstd * (1.0f + sc.w) + sh.w);
+      yr[k] = o;
+    }
+  }
+}
+
 // h[r][n] = sum_k x[r][k] W_in[n][k] + b_in[n] in f32 (K = C is small).  CTA
 // tile: 32 rows x 256 columns, K in chunks of 32 staged in shared memory;
 // each thread accumulates 8 rows x 4 columns, so a k-step costs 8 broadcast
@@ -279,24 +374,29 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
   if (M <= 0) return cudaSuccess;
   if (d % 4 != 0) return cudaErrorInvalidValue;
   const int nv = d / 4;
-  const int grid = (M + LN_WARPS - 1) / LN_WARPS;
   const size_t smem = 2 * static_cast<size_t>(nv) * sizeof(float4);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  const int grid = (M + LN_WARPS - 1) / LN_WARPS;
 #define PSV_LN_LAUNCH(V)                                                                     \
   return launch_pdl(ln_mod_kernel<V>, dim3(grid), dim3(LN_WARPS * 32), smem, st, h, y, M, d, T, \
                     tasks, table, use_fmod, block, shift_off, scale_off, eps)
+#define PSV_LN_WIDE(V, R)                                                                    \
+  return launch_pdl(ln_mod_wide_kernel<V, R>, dim3((M + LN_WARPS / R - 1) / (LN_WARPS / R)),  \
+                    dim3(LN_WARPS * 32), smem, st, h, y, M, d, T, tasks, table, use_fmod, block, \
+                    shift_off, scale_off, eps)
   if (nv <= 32 * 1) PSV_LN_LAUNCH(1);
   else if (nv <= 32 * 2) PSV_LN_LAUNCH(2);
   else if (nv <= 32 * 4) PSV_LN_LAUNCH(4);
   else if (nv <= 32 * 8) PSV_LN_LAUNCH(8);
   else if (nv <= 32 * 12) PSV_LN_LAUNCH(12);
   else if (nv <= 32 * 16) PSV_LN_LAUNCH(16);
-  else if (nv <= 32 * 24) PSV_LN_LAUNCH(24);
-  else if (nv <= 32 * 32) PSV_LN_LAUNCH(32);
-  else if (nv <= 32 * 40) PSV_LN_LAUNCH(40);
-  else if (nv <= 32 * 48) PSV_LN_LAUNCH(48);
+  else if (nv <= 2 * 32 * 12) PSV_LN_WIDE(12, 2);   // d <= 3072
+  else if (nv <= 4 * 32 * 10) PSV_LN_WIDE(10, 4);   // d <= 5120
+  else if (nv <= 4 * 32 * 12) PSV_LN_WIDE(12, 4);
+  else if (nv <= 8 * 32 * 12) PSV_LN_WIDE(12, 8);
   else return cudaErrorInvalidValue;
 #undef PSV_LN_LAUNCH
+#undef PSV_LN_WIDE
   return cudaGetLastError();
 }
 

@@ -622,10 +622,14 @@ def measure_steady(cfg_name: str, local: int, min_seconds: float = 1.5, max_step
     att_us = at.get("total_ms", 0.0) / max(1, at.get("launches", 0)) * 1e3 if at else None
     att_tf = (at["flops"] / at["launches"] / (att_us / 1e6) / 1e12) if at and att_us else None
     roof = wave_roofline(cfg, ms, peaks, peak_src)
+    tot = sum(v["total_ms"] for v in times.values()) or 1e-9
     return {"workload": workload_name(cfg_name, cfg), "steps": steps, "ms_per_chunk": ms,
             "chunks_per_s": n_st / (ms / 1e3), "wave_frac_burst": roof["frac_burst"],
             "wave_frac_sustained": roof["frac_sustained"], "tensor_tflops": roof["tensor_tflops"],
-            "attention_us_per_launch": att_us, "attention_tflops": att_tf}
+            "attention_us_per_launch": att_us, "attention_tflops": att_tf,
+            "kernel_us_per_launch": {k: v["total_ms"] / max(1, v["launches"]) * 1e3
+                                     for k, v in times.items() if v["launches"]},
+            "kernel_share": {k: v["total_ms"] / tot for k, v in times.items() if v["launches"]}}
 
 
 def run_latency(args, cfg_name, cfg, world, rank, local):

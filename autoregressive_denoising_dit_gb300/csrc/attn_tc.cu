@@ -67,6 +67,9 @@ constexpr int kStages = 3;                 // K and V^T stages
 // before the first launch (kRegsNeeded).
 constexpr int kRegsLow = 64, kRegsHigh = 216;
 constexpr int kRegsNeeded = 128 * kRegsLow + 256 * kRegsHigh;
+// Tails of head h are queued after the non-tail pieces of head h + kTailDelay
+// of the same task (see decode_piece).
+constexpr int kTailDelay = 4;
 // Threads of a pair that take each work piece: the even CTA's MMA issuer, and
 // in both CTAs the V^T loader and one softmax thread; the odd CTA's Q/K loader
 // (the even CTA's one publishes the pieces).
@@ -256,25 +259,55 @@ __host__ __device__ __forceinline__ int pieces_tail(int kv_len, int T, int H) {
 }
 
 // Work piece k of the queue -> {task, head, query unit, half | halves << 8};
-// x = -1 past the end.  Order: the non-tail pieces grouped by (task, head)
-// (the pairs that share a K/V window run together while it is in L2), then
-// the tail pieces, so the shortest pieces fill the end of the launch.
+// x = -1 past the end.  Order, task by task: the non-tail pieces of one
+// (task, head) together (the pairs that share its K/V window run at the same
+// time), and the tail pieces of head h after the non-tail pieces of head
+// h + kTailDelay, while head h's window is still in L2 — except for the last
+// F (task, head) groups of the launch, F = half the pairs, whose tails close
+// the queue: short pieces that even out the end of the launch.  (All tails at
+// the end made the tail phase of an 8-stream wave DRAM-bound: every tail half
+// re-read its window; interleaving all of them left long pieces at the end.)
 __device__ int4 decode_piece(int k, const AttnParams& p) {
   if (k < 0 || k >= p.n_pieces) return make_int4(-1, 0, 0, 0);
   const int nu = n_units_of(p.T);
   const bool tail = has_tail(p.T);
   const int nm = nu - (tail ? 1 : 0);
+  const int G = p.n_tasks * p.H;
+  const int pairs = static_cast<int>(gridDim.x / 2);
+  const int F = tail ? min(G, (pairs + 1) / 2) : 0;  // groups whose tails close the queue
+  const int gf = G - F;
+  const int D = min(kTailDelay, p.H);
   for (int t = 0; t < p.n_tasks; ++t) {
-    const int ns = n_splits(p.tasks[t].kv_len, false);
-    const int c = p.H * nm * ns;
-    if (k < c) return make_int4(t, k / (nm * ns), (k / ns) % nm, (k % ns) | (ns << 8));
-    k -= c;
+    const int kv = p.tasks[t].kv_len;
+    const int nsm = n_splits(kv, false), nst = tail ? n_splits(kv, true) : 0;
+    const int a = nm * nsm, b = nst;  // pieces of one head: non-tail, tail
+    const int hf = min(max(gf - t * p.H, 0), p.H);  // heads [0, hf) interleave their tails
+    const int hb = min(hf, p.H - D);                 // ... after the head D further on
+    const int c = p.H * a + hf * b;
+    if (k >= c) {
+      k -= c;
+      continue;
+    }
+    auto main_piece = [&](int h, int i) { return make_int4(t, h, i / nsm, (i % nsm) | (nsm << 8)); };
+    auto tail_piece = [&](int h, int i) { return make_int4(t, h, nu - 1, i | (nst << 8)); };
+    if (k < D * a) return main_piece(k / a, k % a);
+    k -= D * a;
+    if (k < hb * (a + b)) {
+      const int blk = k / (a + b), off = k % (a + b);
+      return off < a ? main_piece(D + blk, off) : tail_piece(blk, off - a);
+    }
+    k -= hb * (a + b);
+    if (k < (p.H - D - hb) * a) return main_piece(D + hb + k / a, k % a);
+    k -= (p.H - D - hb) * a;
+    if (b == 0) break;
+    return tail_piece(hb + k / b, k % b);
   }
   if (tail) {
     for (int t = 0; t < p.n_tasks; ++t) {
-      const int ns = n_splits(p.tasks[t].kv_len, true);
-      const int c = p.H * ns;
-      if (k < c) return make_int4(t, k / ns, nu - 1, (k % ns) | (ns << 8));
+      const int nst = n_splits(p.tasks[t].kv_len, true);
+      const int hf = min(max(gf - t * p.H, 0), p.H);
+      const int c = (p.H - hf) * nst;
+      if (k < c) return make_int4(t, hf + k / nst, nu - 1, (k % nst) | (nst << 8));
       k -= c;
     }
   }

@@ -625,7 +625,18 @@ size_t gemm_smem_bytes() {
 // The wide tile pays off only where the main loop is long against the
 // exposed epilogue: the down-projection (K = F).  Measured on the 1.3B wave:
 // down 100 -> 94 us; QKV 66 -> 92, up 105 -> 130, out-projection 29 -> 31 us.
-bool use_wide(int epi, int K) { return epi == EPI_RESID && K >= 4096; }
+// It also halves the tile count, so it is taken only when its rounds of tiles
+// over the clusters cost less: a wide tile's main loop is about twice a
+// narrow one's, which TMA ingest stretches by ~1.22 (5B down-projection:
+// 84 wide tiles on 76 clusters = 2 rounds, against 3 rounds of narrow ones).
+bool use_wide(int epi, int M, int N, int K, int clusters) {
+  if (epi != EPI_RESID || K < 4096) return false;
+  if (clusters < 1) return true;
+  const int n_mp = ((M + BM - 1) / BM + 1) / 2;
+  const int rounds_w = (n_mp * ((N + 511) / 512) + clusters - 1) / clusters;
+  const int rounds_n = (n_mp * ((N + 255) / 256) + clusters - 1) / clusters;
+  return 2.0 * rounds_w <= 1.22 * rounds_n;
+}
 
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmC, const CUtensorMap* tmD, const CUtensorMap* tmE,
@@ -636,7 +647,7 @@ cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
   const CUtensorMap* dm = tmD ? tmD : tmA;
   const CUtensorMap* em = tmE ? tmE : tmA;
-  const bool wide = use_wide(epi, p.K);
+  const bool wide = use_wide(epi, p.M, p.N, p.K, grid / 2);
   switch (epi) {
     case EPI_QKV:
       return wide ? launch_one<EPI_QKV, true>(tmA, tmB, c, dm, em, p, grid, st)

@@ -210,102 +210,35 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
-// h[r][n] = sum_k x[r][k] W_in[n][k] + b_in[n] in f32 (K = C is small).  CTA
-// tile: 32 rows x 256 columns, K in chunks of 32 staged in shared memory;
-// each thread accumulates 8 rows x 4 columns, so a k-step costs 8 broadcast
-// reads of x and one 16-byte read of W for 32 FMAs (the kernel is bound by
-// the FMA pipe and the write of h), and writes float4 rows.
-constexpr int IP_ROWS = 32, IP_COLS = 256, IP_KC = 32, IP_THREADS = 256;
-constexpr int IP_RG = 8, IP_CG = 4;  // rows, columns per thread
-__global__ void __launch_bounds__(IP_THREADS)
-    in_proj_kernel(const float* __restrict__ state, const __nv_bfloat16* __restrict__ w_in,
-                   const float* __restrict__ b_in, float* __restrict__ h, int M, int d, int C,
-                   int T, const TaskDev* __restrict__ tasks) {
-  __shared__ float xs[IP_ROWS][IP_KC + 1];
-  __shared__ __align__(16) float ws[IP_KC][IP_COLS + 4];  // padded: fewer bank conflicts on the fill
+// Split of the latent rows for the tensor-core in-projection: row r of the
+// wave (task r / T, token r % T) -> [bf16(x) | bf16(x - bf16(x)) | 0 ...].
+// x - bf16(x) is exact in f32, so hi + lo carries x to 2^-17 relative.
+__global__ void in_split_kernel(const float* __restrict__ state, const TaskDev* __restrict__ tasks,
+                                __nv_bfloat16* __restrict__ xs, int M, int C, int T, int K2) {
   pdl_trigger();
   pdl_wait();  // the latent state is the previous wave's output
-  const int r0 = blockIdx.x * IP_ROWS;
-  const int c0 = blockIdx.y * IP_COLS;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 column groups x 4 row groups
-  float acc[IP_RG][IP_CG];
-#pragma unroll
-  for (int i = 0; i < IP_RG; ++i)
-#pragma unroll
-    for (int j = 0; j < IP_CG; ++j) acc[i][j] = 0.0f;
-  // 16-byte loads of x (4 floats) and W (8 bf16) when C allows them
-  const bool vec = (C % 8) == 0;
-  for (int k0 = 0; k0 < C; k0 += IP_KC) {
-    if (vec) {
-      for (int idx = threadIdx.x; idx < IP_ROWS * (IP_KC / 4); idx += IP_THREADS) {
-        const int rr = idx / (IP_KC / 4), kq = idx % (IP_KC / 4);
-        const int row = r0 + rr, k = k0 + kq * 4;
-        float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row < M && k < C) {
-          const TaskDev& t = tasks[row / T];
-          xv = *reinterpret_cast<const float4*>(
-              state + (static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k);
-        }
-        xs[rr][kq * 4] = xv.x;
-        xs[rr][kq * 4 + 1] = xv.y;
-        xs[rr][kq * 4 + 2] = xv.z;
-        xs[rr][kq * 4 + 3] = xv.w;
-      }
-      for (int idx = threadIdx.x; idx < IP_COLS * (IP_KC / 8); idx += IP_THREADS) {
-        const int nn = idx / (IP_KC / 8), kq = idx % (IP_KC / 8);
-        const int col = c0 + nn, k = k0 + kq * 8;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (col < d && k < C) raw = *reinterpret_cast<const uint4*>(w_in + static_cast<int64_t>(col) * C + k);
-        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(w2[e]);
-          ws[kq * 8 + 2 * e][nn] = f.x;
-          ws[kq * 8 + 2 * e + 1][nn] = f.y;
-        }
-      }
-    } else {
-      for (int idx = threadIdx.x; idx < IP_ROWS * IP_KC; idx += IP_THREADS) {
-        const int rr = idx / IP_KC, kk = idx % IP_KC;
-        const int row = r0 + rr, k = k0 + kk;
-        float xv = 0.0f;
-        if (row < M && k < C) {
-          const TaskDev& t = tasks[row / T];
-          xv = state[(static_cast<int64_t>(t.state_slot) * T + (row - t.row0)) * C + k];
-        }
-        xs[rr][kk] = xv;
-      }
-      for (int idx = threadIdx.x; idx < IP_KC * IP_COLS; idx += IP_THREADS) {
-        const int nn = idx / IP_KC, kk = idx % IP_KC;  // k fastest: coalesced weight rows
-        const int col = c0 + nn, k = k0 + kk;
-        ws[kk][nn] = (col < d && k < C) ? __bfloat162float(w_in[static_cast<int64_t>(col) * C + k]) : 0.0f;
-      }
+  const int64_t total = static_cast<int64_t>(M) * K2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / K2), k = static_cast<int>(i % K2);
+    float v = 0.0f;
+    if (k < 2 * C) {
+      const TaskDev& t = tasks[r / T];
+      const float x = state[(static_cast<int64_t>(t.state_slot) * T + (r - t.row0)) * C + (k % C)];
+      const float hi = __bfloat162float(__float2bfloat16_rn(x));
+      v = k < C ? hi : x - hi;
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < IP_KC; ++kk) {
-      const float4 w = *reinterpret_cast<const float4*>(&ws[kk][tx * IP_CG]);
-#pragma unroll
-      for (int i = 0; i < IP_RG; ++i) {
-        const float xv = xs[ty * IP_RG + i][kk];
-        acc[i][0] = fmaf(xv, w.x, acc[i][0]);
-        acc[i][1] = fmaf(xv, w.y, acc[i][1]);
-        acc[i][2] = fmaf(xv, w.z, acc[i][2]);
-        acc[i][3] = fmaf(xv, w.w, acc[i][3]);
-      }
-    }
-    __syncthreads();
+    xs[i] = __float2bfloat16_rn(v);
   }
-  const int n = c0 + tx * IP_CG;
-  if (n < d) {  // d % 4 == 0, so a column group is whole
-    const float4 b = *reinterpret_cast<const float4*>(b_in + n);
-#pragma unroll
-    for (int i = 0; i < IP_RG; ++i) {
-      const int row = r0 + ty * IP_RG + i;
-      if (row < M)
-        *reinterpret_cast<float4*>(h + static_cast<int64_t>(row) * d + n) =
-            make_float4(acc[i][0] + b.x, acc[i][1] + b.y, acc[i][2] + b.z, acc[i][3] + b.w);
-    }
+}
+
+__global__ void build_in2_kernel(const __nv_bfloat16* __restrict__ w_in, __nv_bfloat16* __restrict__ w2,
+                                 int d, int C, int K2, int rows) {
+  const int64_t total = static_cast<int64_t>(rows) * K2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(i / K2), k = static_cast<int>(i % K2);
+    w2[i] = (n < d && k < 2 * C) ? w_in[static_cast<int64_t>(n) * C + (k % C)] : __float2bfloat16_rn(0.0f);
   }
 }
 
@@ -400,13 +333,20 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
   return cudaGetLastError();
 }
 
-cudaError_t launch_in_proj(const float* state, const __nv_bfloat16* w_in, const float* b_in,
-                           float* h, int M, int d, int C, int T, const TaskDev* tasks,
-                           cudaStream_t st) {
+cudaError_t launch_in_split(const float* state, const TaskDev* tasks, __nv_bfloat16* xs, int M,
+                            int C, int T, int K2, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  if (d % 4 != 0) return cudaErrorInvalidValue;
-  dim3 grid((M + IP_ROWS - 1) / IP_ROWS, (d + IP_COLS - 1) / IP_COLS);
-  return launch_pdl(in_proj_kernel, grid, dim3(IP_THREADS), 0, st, state, w_in, b_in, h, M, d, C, T, tasks);
+  const int64_t total = static_cast<int64_t>(M) * K2;
+  const int grid = static_cast<int>((total + 255) / 256 < 1216 ? (total + 255) / 256 : 1216);
+  return launch_pdl(in_split_kernel, dim3(grid), dim3(256), 0, st, state, tasks, xs, M, C, T, K2);
+}
+
+cudaError_t launch_build_in2(const __nv_bfloat16* w_in, __nv_bfloat16* w_in2, int d, int C,
+                             int K2, int rows, cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(rows) * K2;
+  const int grid = static_cast<int>((total + 255) / 256 < 1216 ? (total + 255) / 256 : 1216);
+  build_in2_kernel<<<grid, 256, 0, st>>>(w_in, w_in2, d, C, K2, rows);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat16* W,

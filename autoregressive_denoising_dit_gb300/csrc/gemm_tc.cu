@@ -106,11 +106,38 @@ __device__ __forceinline__ void epilogue32(const GemmParams& p, int row, int n0,
 
   if (EPI == EPI_EULER) {
     // Velocity head: x += dt * (acc + b_out); only the first C columns exist.
-    float* x = p.state + (static_cast<int64_t>(t.state_slot) * p.T + li) * p.C;
+    // Every load of x and b_out is issued before the first store (one
+    // dependent read-modify-write per element would serialise 32 round trips
+    // to memory per row); 16-byte accesses where the row allows them.
+    float* x = p.state + (static_cast<int64_t>(t.state_slot) * p.T + li) * p.C + n0;
+    const float* bn = p.bias + n0;
+    const int nn = p.N - n0 < 32 ? p.N - n0 : 32;
+    if (nn == 32 && (p.C % 4) == 0) {
+      float4 xv[8], bv[8];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int n = n0 + i;
-      if (n < p.N) x[n] += t.dt * (v[i] + p.bias[n]);
+      for (int i = 0; i < 8; ++i) {
+        xv[i] = *reinterpret_cast<const float4*>(x + 4 * i);
+        bv[i] = __ldg(reinterpret_cast<const float4*>(bn) + i);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 r;
+        r.x = xv[i].x + t.dt * (v[4 * i] + bv[i].x);
+        r.y = xv[i].y + t.dt * (v[4 * i + 1] + bv[i].y);
+        r.z = xv[i].z + t.dt * (v[4 * i + 2] + bv[i].z);
+        r.w = xv[i].w + t.dt * (v[4 * i + 3] + bv[i].w);
+        *reinterpret_cast<float4*>(x + 4 * i) = r;
+      }
+    } else {
+      float xv[32], bv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        xv[i] = i < nn ? x[i] : 0.0f;
+        bv[i] = i < nn ? __ldg(bn + i) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nn) x[i] = xv[i] + t.dt * (v[i] + bv[i]);
     }
     return;
   }
@@ -218,6 +245,36 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");
+}
+
+// Plain f32 output of one warp's 32 rows x 32 columns: h = acc + b, staged as
+// a 128-byte-swizzled [32][32] f32 box and written by one TMA store (the
+// in-projection, which writes the residual stream of the wave's rows).
+__device__ __forceinline__ void store_chunk(const GemmParams& p, const CUtensorMap* tmC,
+                                            float* stage, int row0, int n0, float* v) {
+  const int lane = lane_id();
+  if (n0 >= p.N) return;
+  const float4* b4 = reinterpret_cast<const float4*>(p.bias + n0);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 bb = __ldg(b4 + i);
+    v[4 * i] += bb.x;
+    v[4 * i + 1] += bb.y;
+    v[4 * i + 2] += bb.z;
+    v[4 * i + 3] += bb.w;
+  }
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  float4* st4 = reinterpret_cast<float4*>(stage);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st4[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, stage, n0, row0);
+    bulk_commit();
+  }
 }
 
 // GELU of one warp's 32 rows x 64 columns, staged as a 128-byte-swizzled
@@ -544,6 +601,8 @@ __global__ void __launch_bounds__(320, 1)
           tmem_wait_ld();
           if constexpr (EPI == EPI_RESID) {
             resid_chunk(p, &tmC, stage, row, mb * BM + q * 32, nb * BN + ch * 32, v);
+          } else if constexpr (EPI == EPI_STORE) {
+            store_chunk(p, &tmC, stage, mb * BM + q * 32, nb * BN + ch * 32, v);
           } else {
             epilogue32<EPI>(p, row, nb * BN + ch * 32, v);
           }
@@ -556,7 +615,8 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive_remote(tempty0 + acc * 8);  // the even CTA's barrier
     }
     // The staged stores and reductions must have completed before the CTA exits.
-    if ((EPI == EPI_RESID || EPI == EPI_GELU || EPI == EPI_QKV) && lane == 0) bulk_wait_all();
+    if ((EPI == EPI_RESID || EPI == EPI_GELU || EPI == EPI_QKV || EPI == EPI_STORE) && lane == 0)
+      bulk_wait_all();
   }
 
   tc_fence_before();
@@ -641,7 +701,7 @@ bool use_wide(int epi, int M, int N, int K, int clusters) {
 cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
                         const CUtensorMap* tmC, const CUtensorMap* tmD, const CUtensorMap* tmE,
                         const GemmParams& p, int grid, cudaStream_t st) {
-  if ((epi == EPI_RESID || epi == EPI_GELU) && !tmC) return cudaErrorInvalidValue;
+  if ((epi == EPI_RESID || epi == EPI_GELU || epi == EPI_STORE) && !tmC) return cudaErrorInvalidValue;
   if (epi == EPI_QKV && p.d % 64 == 0 && (!tmC || !tmD)) return cudaErrorInvalidValue;
   if (epi == EPI_QKV && p.vt_box && !tmE) return cudaErrorInvalidValue;
   const CUtensorMap* c = tmC ? tmC : tmA;  // unused by the other epilogues
@@ -659,6 +719,7 @@ cudaError_t launch_gemm(int epi, const CUtensorMap* tmA, const CUtensorMap* tmB,
       return wide ? launch_one<EPI_GELU, true>(tmA, tmB, c, dm, em, p, grid, st)
                   : launch_one<EPI_GELU, false>(tmA, tmB, c, dm, em, p, grid, st);
     case EPI_EULER: return launch_one<EPI_EULER, false>(tmA, tmB, c, dm, em, p, grid, st);
+    case EPI_STORE: return launch_one<EPI_STORE, false>(tmA, tmB, c, dm, em, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -52,6 +52,8 @@ struct Layout {
   size_t w_qkv, w_o, w_up, w_down, w_mod;
   size_t b_qkv, b_o, b_up, b_down, b_mod;
   size_t w_in, b_in, w_t1, b_t1, w_t2, b_t2, w_fmod, b_fmod, w_out, b_out;
+  size_t w_in2, xs;  // in-projection operands: [W_in | W_in] and [hi(x) | lo(x)], K2 columns
+  int K2;
   size_t weights_end;
   size_t k_ring, vt_ring, rings_end;
   size_t h, y, q, o, u, acts_end;
@@ -130,6 +132,8 @@ Layout plan_layout(const psv_model_desc& m) {
   L.b_mod = take(B * 6 * d * 4);
   L.w_in = take(d * C * 2);
   L.b_in = take(d * 4);
+  L.K2 = static_cast<int>(round_up(2 * C, 64));
+  L.w_in2 = take(static_cast<size_t>(L.Npad_o) * L.K2 * 2);
   L.w_t1 = take(d * m.t_embed * 2);
   L.b_t1 = take(d * 4);
   L.w_t2 = take(d * d * 2);
@@ -147,6 +151,7 @@ Layout plan_layout(const psv_model_desc& m) {
   L.q = take(static_cast<size_t>(L.M_max) * d * 2);
   L.o = take(static_cast<size_t>(L.M_max) * d * 2);
   L.u = take(static_cast<size_t>(L.M_max) * F * 2);
+  L.xs = take(static_cast<size_t>(L.M_max) * L.K2 * 2);
   L.acts_end = off;
   L.state = take(static_cast<size_t>(L.n_slots) * m.T * C * 4);
   L.mod = take(static_cast<size_t>(L.n_ctabs) * S * B * 6 * d * 4);
@@ -292,6 +297,7 @@ struct psv_ctx {
   std::map<int, WaveStat> wave_stats;  // task count -> steady wave time
   // tensor maps
   CUtensorMap tmA_y, tmA_o, tmA_u, tmB_qkv, tmB_o, tmB_up, tmB_down, tmB_out, tmQ, tmK, tmV;
+  CUtensorMap tmA_xs, tmB_in2;  // in-projection GEMM operands
   CUtensorMap tmC_h;  // f32 h, the target of the gated-residual TMA reductions
   CUtensorMap tmC_u;  // bf16 u, written by the GELU epilogue's TMA stores
   CUtensorMap tmC_q;  // bf16 q and the K ring, written by the QKV epilogue's
@@ -489,10 +495,24 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
   Launcher run{ctx, prof, st};
   const double Md = static_cast<double>(M) * d;
 
-  run.run(K_IN_PROJ, 2.0 * M * m.C * d, M * (m.C + d) * 4.0, [&] {
-    return psv::launch_in_proj(ctx->at<float>(L.state), ctx->at<__nv_bfloat16>(L.w_in),
-                               ctx->at<float>(L.b_in), ctx->at<float>(L.h), M, d, m.C, m.T, tasks, st);
+  // In-projection on the tensor cores: split x into bf16 hi + lo, then
+  // h = [hi | lo] [W_in | W_in]^T + b_in, stored in f32.
+  run.run(K_IN_PROJ, 0.0, M * m.C * 4.0 + static_cast<double>(M) * L.K2 * 2, [&] {
+    return psv::launch_in_split(ctx->at<float>(L.state), tasks, ctx->at<__nv_bfloat16>(L.xs), M, m.C,
+                                m.T, L.K2, st);
   });
+  {
+    psv::GemmParams p = base_gemm(ctx, M);
+    p.N = d;
+    p.K = L.K2;
+    p.block = 0;
+    p.wz = 0;
+    p.bias = ctx->at<float>(L.b_in);
+    run.run(K_IN_PROJ, 2.0 * M * m.C * d, static_cast<double>(M) * L.K2 * 2 + static_cast<double>(M) * d * 4, [&] {
+      return psv::launch_gemm(psv::EPI_STORE, &ctx->tmA_xs, &ctx->tmB_in2, &ctx->tmC_h, nullptr, nullptr, p,
+                              gemm_grid(ctx, M, p.N), st);
+    });
+  }
 
   double attn_flops = 0.0, attn_bytes = 0.0;
   std::vector<int> kv_lens;
@@ -796,6 +816,11 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
       ok &= encode_bf16(&ctx->tmA_o, 2, ctx->arena + L.o, dims, str, box, SW128);
     }
     {
+      uint64_t dims[2] = {static_cast<uint64_t>(L.K2), Mx}, str[1] = {static_cast<uint64_t>(L.K2) * 2};
+      uint32_t box[2] = {64, 128};
+      ok &= encode_bf16(&ctx->tmA_xs, 2, ctx->arena + L.xs, dims, str, box, SW128);
+    }
+    {
       uint64_t dims[2] = {F, Mx}, str[1] = {F * 2};
       uint32_t box[2] = {64, 128};
       ok &= encode_bf16(&ctx->tmA_u, 2, ctx->arena + L.u, dims, str, box, SW128);
@@ -819,6 +844,7 @@ PSV_API int psv_create(const psv_model_desc* desc, void* dev_arena, size_t arena
     ok &= wmap(&ctx->tmB_up, L.w_up, d, L.Npad_up, m.B);
     ok &= wmap(&ctx->tmB_down, L.w_down, F, L.Npad_down, m.B);
     ok &= wmap(&ctx->tmB_out, L.w_out, d, L.Npad_out, 1);
+    ok &= wmap(&ctx->tmB_in2, L.w_in2, L.K2, L.Npad_o, 1);
     const uint32_t aw = m.dh < 64 ? m.dh : 64;
     const CUtensorMapSwizzle swq = aw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : SW128;
     {
@@ -953,6 +979,11 @@ PSV_API int psv_load_weights(psv_ctx* ctx, const psv_weight* w, int n) {
     } else {
       return set_err(ctx, PSV_EINVAL, "weight %d: bad location", i);
     }
+    if (x.id == PSV_W_IN_W)
+      CK(psv::launch_build_in2(reinterpret_cast<const __nv_bfloat16*>(ctx->arena + L.w_in),
+                               reinterpret_cast<__nv_bfloat16*>(ctx->arena + L.w_in2), static_cast<int>(d),
+                               static_cast<int>(C), L.K2, L.Npad_o, ctx->stream),
+         "in-projection weight build");
     if (global) ctx->w_loaded[x.id] = true;
     else ctx->blk_loaded[static_cast<size_t>(x.block) * 16 + (x.id - PSV_W_QKV_W)] = 1;
   }

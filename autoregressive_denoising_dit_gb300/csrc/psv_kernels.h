@@ -40,6 +40,7 @@ enum GemmEpilogue : int {
   EPI_RESID = 1,  // h += gate[task] * C   (gated residual, f32)
   EPI_GELU = 2,   // u = bf16(GELU_tanh(C))
   EPI_EULER = 3,  // x[task] += dt[task] * C   (velocity head + Euler step)
+  EPI_STORE = 4,  // h = C + bias (f32, through TMA stores; the in-projection)
 };
 
 struct GemmParams {
@@ -141,10 +142,15 @@ cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
                           const TaskDev* tasks, const float* table, int use_fmod, int block,
                           int shift_off, int scale_off, float eps, cudaStream_t st);
-// h = x W_in^T + b_in, x gathered from each task's latent state slot.
-cudaError_t launch_in_proj(const float* state, const __nv_bfloat16* w_in, const float* b_in,
-                           float* h, int M, int d, int C, int T, const TaskDev* tasks,
-                           cudaStream_t st);
+// In-projection h = x W_in^T + b_in on the tensor cores: x (f32, gathered
+// from each task's latent state slot) is split into bf16 hi + lo parts,
+// xs[r] = [hi(x_r) | lo(x_r) | 0...] (K2 columns), so that a bf16 GEMM
+// against W2 = [W_in | W_in | 0...] gives x W_in^T to ~2^-17 relative.
+cudaError_t launch_in_split(const float* state, const TaskDev* tasks, __nv_bfloat16* xs, int M,
+                            int C, int T, int K2, cudaStream_t st);
+// W2 [rows][K2] = [W_in | W_in | 0...] from W_in [d][C] (rows >= d: zero).
+cudaError_t launch_build_in2(const __nv_bfloat16* w_in, __nv_bfloat16* w_in2, int d, int C,
+                             int K2, int rows, cudaStream_t st);
 // out[r][n] = act(in[r]) . W[n] + b[n] (+ add[n]), r < R; act = SiLU or id.
 cudaError_t launch_cond_linear(const float* in, int R, int K, const __nv_bfloat16* W,
                                const float* b, const float* add, float* out, int N,

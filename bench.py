@@ -530,7 +530,7 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "chunks/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s / e2e_steps * 1e3},
-        "gpu_launches": (3 + 7 * cfg["B"]) * args.steps,
+        "gpu_launches": (4 + 7 * cfg["B"]) * args.steps,
         "clocks": clk,
         # a chunk's S steps run in S consecutive steady waves
         "response_ms": S * ms_step,
@@ -710,7 +710,7 @@ def run_latency(args, cfg_name, cfg, world, rank, local):
         "e2e": {"value": world * n_st / (e2e_ms / 1e3), "unit": "chunks/s",
                 "h2d_bytes_per_step": n_st * T * C * 4, "d2h_bytes_per_step": n_st * T * C * 4,
                 "response_ms": e2e_ms},
-        "gpu_launches": (3 + 7 * cfg["B"]) * S * args.steps,
+        "gpu_launches": (4 + 7 * cfg["B"]) * S * args.steps,
         "clocks": clk,
     }
     sess.close()

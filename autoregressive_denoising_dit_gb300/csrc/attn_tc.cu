@@ -263,10 +263,13 @@ __host__ __device__ __forceinline__ int pieces_tail(int kv_len, int T, int H) {
 // (task, head) together (the pairs that share its K/V window run at the same
 // time), and the tail pieces of head h after the non-tail pieces of head
 // h + kTailDelay, while head h's window is still in L2 — except for the last
-// F (task, head) groups of the launch, F = half the pairs, whose tails close
-// the queue: short pieces that even out the end of the launch.  (All tails at
-// the end made the tail phase of an 8-stream wave DRAM-bound: every tail half
-// re-read its window; interleaving all of them left long pieces at the end.)
+// F (task, head) groups of the launch, F = a quarter of the pairs, whose tails
+// close the queue: short pieces that even out the end of the launch, and few
+// enough that the windows of those last groups are still in L2 when their
+// tails run.  (All tails at the end made the tail phase of an 8-stream wave
+// DRAM-bound: every tail half re-read its window; interleaving all of them
+// left long pieces at the end; with F = half the pairs the final tails
+// re-read ~120 MB of a 1.3B-shaped launch's 211 MB of Q, K and V.)
 __device__ int4 decode_piece(int k, const AttnParams& p) {
   if (k < 0 || k >= p.n_pieces) return make_int4(-1, 0, 0, 0);
   const int nu = n_units_of(p.T);
@@ -274,7 +277,7 @@ __device__ int4 decode_piece(int k, const AttnParams& p) {
   const int nm = nu - (tail ? 1 : 0);
   const int G = p.n_tasks * p.H;
   const int pairs = static_cast<int>(gridDim.x / 2);
-  const int F = tail ? min(G, (pairs + 1) / 2) : 0;  // groups whose tails close the queue
+  const int F = tail ? min(G, (pairs + 3) / 4) : 0;  // groups whose tails close the queue
   const int gf = G - F;
   const int D = min(kTailDelay, p.H);
   for (int t = 0; t < p.n_tasks; ++t) {

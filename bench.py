@@ -429,10 +429,12 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
     # inputs to the device (submit) and reads its outputs back (poll).
     inputs = {}
 
-    def e2e_step(c):
+    def e2e_submit(c):
         for st, sid in zip(streams, sids):
             sess.submit(sid, inputs[(c, sid)] if (c, sid) in inputs else st.noise(c))
         sess.run_wave()
+
+    def e2e_poll():
         out = 0
         for sid in sids:
             while True:
@@ -459,12 +461,25 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
             inputs[(c, sid)] = np.ascontiguousarray(st.noise(c), dtype=np.float32)
     barrier(world)
     torch.cuda.synchronize()
+    # As a server runs it: the next wave (its inputs copied in) is enqueued
+    # before the previous wave's outputs are read back, so the device does not
+    # wait for the host between waves.  Every one of the K steps' input copies,
+    # waves and output reads is inside the clock.
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
     w0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step(next_chunk)
-        next_chunk += 1
+    emitted = 0
+    e2e_submit(next_chunk)
+    for k in range(1, e2e_steps):
+        e2e_submit(next_chunk + k)
+        emitted += e2e_poll()
+    emitted += e2e_poll()
+    next_chunk += e2e_steps
     torch.cuda.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - w0, world, dev)
+    e2e_s_local = time.perf_counter() - w0
+    e2e_clk = e2e_clocks.stop()
+    assert emitted == n_st * e2e_steps, f"end-to-end phase emitted {emitted} chunks"
+    e2e_s = max_over_ranks(e2e_s_local, world, dev)
     e2e_value = world * n_st * e2e_steps / e2e_s
     n_task = S * n_st
     h2d = n_st * T * C * 4 + n_task * 48 + n_st * (cfg["dh"] // 2) * 8
@@ -529,7 +544,10 @@ def run_psv(args, cfg_name, cfg, world, rank, local):
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "chunks/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s / e2e_steps * 1e3},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s / e2e_steps * 1e3,
+                # the SM clock under the power cap during this phase (it runs
+                # after the device-timed one; a hotter chip clocks lower)
+                "clocks": {k: (e2e_clk or {}).get(k) for k in ("sm_mhz", "sm_mhz_min", "reasons", "samples")}},
         "gpu_launches": (4 + 7 * cfg["B"]) * args.steps,
         "clocks": clk,
         # a chunk's S steps run in S consecutive steady waves

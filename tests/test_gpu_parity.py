@@ -48,6 +48,35 @@ def test_mid_two_streams_ragged_tiles_match_oracle():
     _compare(cfg, w, streams, cfg["n_chunks"])
 
 
+ODD = dict(d=384, H=3, T=101, C=30, n_chunks=5)
+
+
+def test_odd_shapes_match_oracle():
+    """T = 101: the 32-row warps of the QKV epilogue straddle tasks and the end of the
+    wave, ring rows start unaligned (K and V^T appended row by row), one 101-row tail
+    unit per task and a 47-key last key tile; C = 30: the velocity head's scalar path
+    and the in-projection's split padded from 60 to 64 columns; d = 384 (3 heads): the
+    GEMMs' last column tiles are half empty (N = 384, 1152, 30)."""
+    cfg = synth.config("mid", **ODD)
+    w = synth.make_weights(cfg, 0)
+    streams = synth.make_streams(cfg)
+    _compare(cfg, w, streams, cfg["n_chunks"])
+
+
+def test_odd_shapes_wave_order_equals_sequential_order_bitwise():
+    cfg = synth.config("mid", **ODD)
+    w = synth.make_weights(cfg, 0)
+    streams = synth.make_streams(cfg)
+    from autoregressive_denoising_dit_gb300 import _psv as P
+
+    batched, _ = run_gpu(cfg, w, streams, 4)
+    seq, waves = run_gpu(cfg, w, streams, 4, flags=P.PSV_FLAG_SEQUENTIAL)
+    assert waves == 2 * 4 * cfg["S"]
+    for i in range(2):
+        for c in range(4):
+            np.testing.assert_array_equal(batched[i][c], seq[i][c])
+
+
 def test_wave_order_equals_sequential_order_bitwise():
     cfg = synth.config("mid")
     w = synth.make_weights(cfg, 0)

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 
 // Split of the latent rows for the tensor-core in-projection: row r of the
 // wave (task r / T, token r % T) -> [bf16(x) | bf16(x - bf16(x)) | 0 ...].
-// x - bf16(x) is exact in f32, so hi + lo carries x to 2^-17 relative.
+// x - bf16(x) is exact in f32, so hi + lo carries x to within 2^-16 relative.
 __global__ void in_split_kernel(const float* __restrict__ state, const TaskDev* __restrict__ tasks,
                                 __nv_bfloat16* __restrict__ xs, int M, int C, int T, int K2) {
   pdl_trigger();

@@ -145,7 +145,7 @@ cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
 // In-projection h = x W_in^T + b_in on the tensor cores: x (f32, gathered
 // from each task's latent state slot) is split into bf16 hi + lo parts,
 // xs[r] = [hi(x_r) | lo(x_r) | 0...] (K2 columns), so that a bf16 GEMM
-// against W2 = [W_in | W_in | 0...] gives x W_in^T to ~2^-17 relative.
+// against W2 = [W_in | W_in | 0...] gives x W_in^T with x kept to 2^-16 relative.
 cudaError_t launch_in_split(const float* state, const TaskDev* tasks, __nv_bfloat16* xs, int M,
                             int C, int T, int K2, cudaStream_t st);
 // W2 [rows][K2] = [W_in | W_in | 0...] from W_in [d][C] (rows >= d: zero).

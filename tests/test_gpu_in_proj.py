@@ -3,9 +3,9 @@
 h = x W_inᵀ + b_in opens every (chunk, step) task (BAAI announcement, Fig. 1: each
 chunk is denoised from its submitted noise); x is the f32 latent, W_in bf16.  The
 library runs it as one bf16 GEMM of [hi(x) | lo(x)] against [W_in | W_in], with
-hi = bf16(x) and lo = bf16(x - hi): x - hi is exact in f32 and lo keeps it to 2^-8
-relative, so hi + lo carries x to ~2^-17 relative and each product with a bf16 weight
-is exact in the f32 accumulator.  The result must therefore match the f64 definition
+hi = bf16(x) and lo = bf16(x - hi): x - hi is exact in f32 and at most 2^-8 |x|, and
+lo keeps it to 2^-8 relative, so hi + lo carries x to within 2^-16 relative and each
+product with a bf16 weight is exact in the f32 accumulator.  The result must therefore match the f64 definition
 to f32 accumulation error, two orders of magnitude tighter than a plain bf16 product
 of x (~4e-3 relative).  The block-0 tap of the first wave (one task: chunk 0, step 0)
 captures h as the in-projection wrote it.

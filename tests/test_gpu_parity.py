@@ -63,6 +63,15 @@ def test_odd_shapes_match_oracle():
     _compare(cfg, w, streams, cfg["n_chunks"])
 
 
+def test_one_step_one_block_dh64_match_oracle():
+    """S = 1 (each chunk denoised in a single Euler step from t = 1 to 0, so every
+    wave holds one task per stream), B = 1, and 64-wide heads (H = 4)."""
+    cfg = synth.config("mid", S=1, B=1, H=4, dh=64, n_chunks=4)
+    w = synth.make_weights(cfg, 0)
+    streams = synth.make_streams(cfg)
+    _compare(cfg, w, streams, cfg["n_chunks"])
+
+
 def test_odd_shapes_wave_order_equals_sequential_order_bitwise():
     cfg = synth.config("mid", **ODD)
     w = synth.make_weights(cfg, 0)

@@ -115,6 +115,139 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
+// The LayerNorm of rows of up to 2048 values, staged by bulk copies: one
+// persistent CTA per SM takes a contiguous block of rows (so the rows of at
+// most two tasks: their shift / scale vectors are copied to shared memory
+// first), brought in by cp.async.bulk in batches of half the staging area,
+// the next batch's copies in flight while 16 warps normalise the current one
+// (one row per warp, in registers).  Every row is computed with the order of
+// operations of ln_mod_kernel, so the two kernels give the same bits.
+constexpr int LNB_WARPS = 16;
+constexpr uint32_t LNB_SMEM = 200 * 1024;
+
+__device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int MAXV>
+__global__ void __launch_bounds__(LNB_WARPS * 32, 1)
+    ln_bulk_kernel(const float* __restrict__ h, __nv_bfloat16* __restrict__ y, int M, int d, int T,
+                   const TaskDev* __restrict__ tasks, const float* __restrict__ table, int use_fmod,
+                   int block, int shift_off, int scale_off, float eps, int* err) {
+  extern __shared__ __align__(128) uint8_t lnb_smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lnb_smem);          // [2]
+  float4* tab = reinterpret_cast<float4*>(lnb_smem + 128);           // [task a, b][shift, scale][d / 4]
+  const int warp = warp_id(), lane = lane_id();
+  const int nv = d >> 2;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * 4;
+  uint8_t* rows_area = lnb_smem + 128 + 4 * row_bytes;
+  const uint32_t half = ((LNB_SMEM - 128 - 4 * row_bytes) / 2) & ~15u;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  pdl_trigger();
+  pdl_wait();  // h is the previous kernel's output
+  __syncthreads();
+  const int per = (M + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int r0 = min(M, static_cast<int>(blockIdx.x) * per), r1 = min(M, r0 + per);
+  if (r0 >= r1) return;
+  const int batch = static_cast<int>(half / row_bytes);
+  const int nbatch = (r1 - r0 + batch - 1) / batch;
+  auto vec_base = [&](int ti) {
+    const TaskDev& t = tasks[ti];
+    return table + (use_fmod ? static_cast<int64_t>(t.fmod0)
+                             : static_cast<int64_t>(t.mod0) + static_cast<int64_t>(block) * 6 * d);
+  };
+  auto issue = [&](int k) {
+    const int b0 = r0 + k * batch, nb = min(batch, r1 - b0);
+    uint8_t* buf = rows_area + (k & 1) * half;
+    mbar_arrive_expect_tx(&bars[k & 1], static_cast<uint32_t>(nb) * row_bytes);
+    for (int i = 0; i < nb; ++i)
+      bulk_load_g2s(buf + i * row_bytes, h + static_cast<int64_t>(b0 + i) * d, row_bytes, &bars[k & 1]);
+  };
+  if (threadIdx.x == 0) issue(0);
+  const int ta = r0 / T, tb = (r1 - 1) / T;
+  for (int idx = threadIdx.x; idx < 4 * nv; idx += LNB_WARPS * 32) {
+    const int which = idx / nv, c = idx - which * nv;  // which: task (bit 1), scale (bit 0)
+    tab[idx] = __ldg(reinterpret_cast<const float4*>(vec_base((which & 2) ? tb : ta) +
+                                                     ((which & 1) ? scale_off : shift_off)) + c);
+  }
+  int issued = 1;
+  bool ok = true;
+  for (int k = 0; k < nbatch; ++k) {
+    if (k + 1 < nbatch) {
+      if (threadIdx.x == 0) {  // buffer (k+1)&1 was released at the end of batch k-1
+        fence_proxy_async_smem();
+        issue(k + 1);
+      }
+      ++issued;
+    }
+    // (the first wait also orders the table fill above before its use)
+    ok = __syncthreads_and(mbar_wait(&bars[k & 1], (k >> 1) & 1, err, ERR_LN_TIMEOUT) ? 1 : 0) != 0;
+    if (!ok) break;
+    const int b0 = r0 + k * batch, nb = min(batch, r1 - b0);
+    const uint8_t* buf = rows_area + (k & 1) * half;
+    for (int i = warp; i < nb; i += LNB_WARPS) {
+      const int row = b0 + i;
+      const float4* hr = reinterpret_cast<const float4*>(buf + i * row_bytes);
+      float4 v[MAXV];
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = lane + j * 32;
+        if (c < nv) {
+          v[j] = hr[c];
+          s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+        }
+      }
+      const float mean = warp_sum(s) / static_cast<float>(d);
+      float q = 0.0f;
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = lane + j * 32;
+        if (c < nv) {
+          const float a = v[j].x - mean, b = v[j].y - mean, cc = v[j].z - mean, e = v[j].w - mean;
+          q += (a * a + b * b) + (cc * cc + e * e);
+        }
+      }
+      const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(d) + eps);
+      const int ti = row / T;
+      const float4* shift = tab + (ti == ta ? 0 : 2) * nv;
+      const float4* scale = shift + nv;
+      if (ti != ta && ti != tb) {  // only when a CTA's rows span more than two tasks
+        shift = reinterpret_cast<const float4*>(vec_base(ti) + shift_off);
+        scale = reinterpret_cast<const float4*>(vec_base(ti) + scale_off);
+      }
+      uint2* yr = reinterpret_cast<uint2*>(y + static_cast<int64_t>(row) * d);
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int c = lane + j * 32;
+        if (c < nv) {
+          const float4 sh = shift[c], sc = scale[c];
+          uint2 o;
+          o.x = pack_bf16x2((v[j].x - mean) * rstd * (1.0f + sc.x) + sh.x,
+                            (v[j].y - mean) * rstd * (1.0f + sc.y) + sh.y);
+          o.y = pack_bf16x2((v[j].z - mean) * rstd * (1.0f + sc.z) + sh.z,
+                            (v[j].w - mean) * rstd * (1.0f + sc.w) + sh.w);
+          yr[c] = o;
+        }
+      }
+    }
+    __syncthreads();  // batch k's buffer is refilled by batch k + 2
+  }
+  if (!ok && threadIdx.x == 0) {
+    // Let this CTA's copies still in flight land before it leaves (bounded).
+    const uint64_t t0 = global_timer_ns();
+    for (int k = 0; k < issued; ++k)
+      while (!mbar_try_wait(&bars[k & 1], (k >> 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {
+      }
+  }
+}
+
 // The same LayerNorm for wide rows (d > 2048): ROWW warps share a row, each
 // holding up to MAXV float4 per lane (interleaved, so every warp load is 512
 // contiguous bytes), and the row's partial sums meet in shared memory in a
@@ -303,10 +436,37 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
 
 cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
                           const TaskDev* tasks, const float* table, int use_fmod, int block,
-                          int shift_off, int scale_off, float eps, cudaStream_t st) {
+                          int shift_off, int scale_off, float eps, int* err, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   if (d % 4 != 0) return cudaErrorInvalidValue;
   const int nv = d / 4;
+  if (d <= 2048 && err) {
+    static uint64_t set_up = 0;
+    static int sms[64] = {};
+    cudaError_t e = once_per_device(&set_up, [&](int dev) {
+      cudaError_t r = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (r != cudaSuccess) return r;
+#define PSV_LNB_ATTR(V)                                                                        \
+  if ((r = cudaFuncSetAttribute(ln_bulk_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                static_cast<int>(LNB_SMEM))) != cudaSuccess)                    \
+    return r;
+      PSV_LNB_ATTR(4) PSV_LNB_ATTR(8) PSV_LNB_ATTR(12) PSV_LNB_ATTR(16)
+#undef PSV_LNB_ATTR
+      return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    const int grid = M < sms[dev] ? M : sms[dev];
+#define PSV_LNB_LAUNCH(V)                                                                   \
+  return launch_pdl(ln_bulk_kernel<V>, dim3(grid), dim3(LNB_WARPS * 32), LNB_SMEM, st, h, y, M, d, \
+                    T, tasks, table, use_fmod, block, shift_off, scale_off, eps, err)
+    if (nv <= 32 * 4) PSV_LNB_LAUNCH(4);
+    else if (nv <= 32 * 8) PSV_LNB_LAUNCH(8);
+    else if (nv <= 32 * 12) PSV_LNB_LAUNCH(12);
+    else PSV_LNB_LAUNCH(16);
+#undef PSV_LNB_LAUNCH
+  }
   const size_t smem = 2 * static_cast<size_t>(nv) * sizeof(float4);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
   const int grid = (M + LN_WARPS - 1) / LN_WARPS;

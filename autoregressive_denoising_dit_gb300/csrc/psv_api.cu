@@ -530,7 +530,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     // LN1 + modulation
     run.run(K_LN, 0, Md * 6.0, [&] {
       return psv::launch_ln_mod(ctx->at<float>(L.h), ctx->at<__nv_bfloat16>(L.y), M, d, m.T, tasks,
-                                ctx->at<float>(L.mod), 0, b, 0, d, m.ln_eps, st);
+                                ctx->at<float>(L.mod), 0, b, 0, d, m.ln_eps, ctx->at<int>(L.err), st);
     });
     // QKV + RoPE + KV append
     {
@@ -593,7 +593,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
     // LN2 + modulation
     run.run(K_LN, 0, Md * 6.0, [&] {
       return psv::launch_ln_mod(ctx->at<float>(L.h), ctx->at<__nv_bfloat16>(L.y), M, d, m.T, tasks,
-                                ctx->at<float>(L.mod), 0, b, 3 * d, 4 * d, m.ln_eps, st);
+                                ctx->at<float>(L.mod), 0, b, 3 * d, 4 * d, m.ln_eps, ctx->at<int>(L.err), st);
     });
     // up + GELU
     {
@@ -629,7 +629,7 @@ cudaError_t enqueue_wave(psv_ctx* ctx, cudaStream_t st, int n, bool prof, bool t
   // final adaLN + velocity head + Euler update
   run.run(K_LN, 0, Md * 6.0, [&] {
     return psv::launch_ln_mod(ctx->at<float>(L.h), ctx->at<__nv_bfloat16>(L.y), M, d, m.T, tasks,
-                              ctx->at<float>(L.fmod), 1, 0, 0, d, m.ln_eps, st);
+                              ctx->at<float>(L.fmod), 1, 0, 0, d, m.ln_eps, ctx->at<int>(L.err), st);
   });
   {
     psv::GemmParams p = base_gemm(ctx, M);
@@ -673,6 +673,7 @@ int read_device_error(psv_ctx* ctx) {
     return set_err(ctx, PSV_EDEVICE, "device error word set: %d (%s)", v,
                    v == psv::ERR_GEMM_TIMEOUT ? "GEMM pipeline wait timed out"
                    : v == psv::ERR_ATTN_TIMEOUT ? "attention pipeline wait timed out"
+                   : v == psv::ERR_LN_TIMEOUT   ? "LayerNorm row copy wait timed out"
                                                 : "bounds check");
   }
   return PSV_OK;

@@ -32,6 +32,7 @@ enum : int {
   ERR_GEMM_TIMEOUT = 1,
   ERR_ATTN_TIMEOUT = 2,
   ERR_BOUNDS = 3,
+  ERR_LN_TIMEOUT = 4,
 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.

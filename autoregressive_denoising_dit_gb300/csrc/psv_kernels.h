@@ -139,9 +139,11 @@ cudaError_t launch_attention(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // Memory-bound kernels.
 // y = bf16(LN(h) * (1 + scale) + shift), per row; shift/scale of the row's
 // task at mod + task.mod0 + block*6d + {shift_off, scale_off} (or fmod).
+// err: the device error word its bounded waits raise (rows of up to 2048
+// values are staged by bulk copies; null: the register kernel only).
 cudaError_t launch_ln_mod(const float* h, __nv_bfloat16* y, int M, int d, int T,
                           const TaskDev* tasks, const float* table, int use_fmod, int block,
-                          int shift_off, int scale_off, float eps, cudaStream_t st);
+                          int shift_off, int scale_off, float eps, int* err, cudaStream_t st);
 // In-projection h = x W_in^T + b_in on the tensor cores: x (f32, gathered
 // from each task's latent state slot) is split into bf16 hi + lo parts,
 // xs[r] = [hi(x_r) | lo(x_r) | 0...] (K2 columns), so that a bf16 GEMM
